@@ -1,0 +1,222 @@
+"""Python access to the CPU oracle (liboracle.so, built from fp8q_oracle.c).
+
+TEST INFRASTRUCTURE ONLY.  Imported by the tests, by the smoke check and by
+the benchmark's CPU-baseline / reference leg; never by the product package.
+The oracle shares no code with the CUDA library: it is plain single-threaded
+C, compiled here with gcc, and every function states the arithmetic it
+follows in fp8q_oracle.c.
+
+Arrays are numpy: bf16 as uint16 bit patterns, e4m3 as uint8 codes, scales
+as float32.  Scale layout: ``col_major=False`` -> s[t*G + g],
+``col_major=True`` -> s[g*T + t].
+"""
+
+from __future__ import annotations
+
+import contextlib
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fp8q_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+SCALE_EPS = np.float32(1e-10)
+RMS_EPS = np.float32(1e-6)
+
+CFLAGS = [
+    "-O2",
+    "-std=c11",
+    "-fPIC",
+    "-shared",
+    "-ffp-contract=off",
+    "-fno-fast-math",
+    "-frounding-math",
+    "-fexcess-precision=standard",
+    "-Wall",
+    "-Wextra",
+]
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so in place with gcc (seconds).  Returns its path."""
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(os.path.join(_HERE, "fp8q_oracle.h")))
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest:
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def compile_variant(source_text: str, out_path: str) -> str:
+    """Compile a modified copy of the oracle source (used by the tests that
+    plant a mistake in the oracle to show that the pins catch it)."""
+    src = out_path + ".c"
+    with open(src, "w") as f:
+        f.write(source_text)
+    subprocess.run(["gcc", *CFLAGS, "-w", "-I", _HERE, "-o", out_path, src, "-lm"], check=True)
+    return out_path
+
+
+def source_text() -> str:
+    with open(_SRC) as f:
+        return f.read()
+
+
+@contextlib.contextmanager
+def use_library(path: str):
+    """Route every oracle call to another build of the oracle for a while."""
+    global _lib
+    old = _lib
+    _lib = _configure(ctypes.CDLL(path))
+    try:
+        yield
+    finally:
+        _lib = old
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        build()
+        _lib = _configure(ctypes.CDLL(_LIB))
+    return _lib
+
+
+def _configure(L: ctypes.CDLL) -> ctypes.CDLL:
+    P = ctypes.c_void_p
+    I64 = ctypes.c_int64
+    F = ctypes.c_float
+    I = ctypes.c_int
+    L.oracle_per_token_group_quant.argtypes = [P, P, P, P, I64, I64, I64, F, I, I]
+    L.oracle_rms_norm_per_block_quant.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, F, I, I]
+    L.oracle_silu_and_mul_per_block_quant.argtypes = [P, P, P, P, I64, I64, I64, F, I, I]
+    for name in ("oracle_per_token_group_quant", "oracle_rms_norm_per_block_quant",
+                 "oracle_silu_and_mul_per_block_quant"):
+        getattr(L, name).restype = I
+    L.oracle_f32_to_e4m3_n.argtypes = [P, P, I64]
+    L.oracle_ue8m0_ceil_n.argtypes = [P, P, I64]
+    L.oracle_silu_mul_n.argtypes = [P, P, P, I64]
+    L.oracle_quant_pairs.argtypes = [P, P, P, I64]
+    L.oracle_row_sumsq.argtypes = [P, I64, I64, P]
+    L.oracle_rms_inv.argtypes = [F, I64, F]
+    L.oracle_rms_inv.restype = F
+    L.oracle_f32_to_bf16.argtypes = [F]
+    L.oracle_f32_to_bf16.restype = ctypes.c_uint16
+    return L
+
+
+def _p(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u16(x) -> np.ndarray:
+    x = np.ascontiguousarray(x)
+    assert x.dtype == np.uint16, x.dtype
+    return x
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (status {rc})")
+
+
+def _scale_shape(T, G, col_major):
+    return (G, T) if col_major else (T, G)
+
+
+def per_token_group_quant(x_bits, group=128, eps=SCALE_EPS, ue8m0=False, col_major=False):
+    """op A.  x_bits uint16 [T,H].  Returns (q uint8 [T,H], scales, scales_pre)."""
+    x = _u16(x_bits)
+    T, H = x.shape
+    G = H // group
+    q = np.empty((T, H), np.uint8)
+    s = np.empty(_scale_shape(T, G, col_major), np.float32)
+    sp = np.empty_like(s)
+    _check(lib().oracle_per_token_group_quant(_p(x), _p(q), _p(s), _p(sp), T, H, group,
+                                              float(eps), int(ue8m0), int(col_major)))
+    return q, s, sp
+
+
+def rms_norm_per_block_quant(x_bits, w_bits, residual_bits=None, group=128, eps=RMS_EPS,
+                             ue8m0=False, col_major=False):
+    """op B.  Returns (q, scales, scales_pre, inv [T], residual_out or None)."""
+    x = _u16(x_bits)
+    w = _u16(w_bits)
+    T, H = x.shape
+    G = H // group
+    q = np.empty((T, H), np.uint8)
+    s = np.empty(_scale_shape(T, G, col_major), np.float32)
+    sp = np.empty_like(s)
+    inv = np.empty(T, np.float32)
+    r = None
+    if residual_bits is not None:
+        r = np.array(_u16(residual_bits), copy=True)
+    _check(lib().oracle_rms_norm_per_block_quant(
+        _p(x), _p(r) if r is not None else None, _p(w), _p(q), _p(s), _p(sp), _p(inv),
+        T, H, group, float(eps), int(ue8m0), int(col_major)))
+    return q, s, sp, inv, r
+
+
+def silu_and_mul_per_block_quant(x_bits, group=128, eps=SCALE_EPS, ue8m0=False, col_major=False):
+    """op C.  x_bits uint16 [T, 2I].  Returns (q uint8 [T,I], scales, scales_pre)."""
+    x = _u16(x_bits)
+    T, H2 = x.shape
+    I = H2 // 2
+    G = I // group
+    q = np.empty((T, I), np.uint8)
+    s = np.empty(_scale_shape(T, G, col_major), np.float32)
+    sp = np.empty_like(s)
+    _check(lib().oracle_silu_and_mul_per_block_quant(_p(x), _p(q), _p(s), _p(sp), T, I, group,
+                                                     float(eps), int(ue8m0), int(col_major)))
+    return q, s, sp
+
+
+def f32_to_e4m3(v) -> np.ndarray:
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.empty(v.shape, np.uint8)
+    lib().oracle_f32_to_e4m3_n(_p(v), _p(out), v.size)
+    return out
+
+
+def ue8m0_ceil(s) -> np.ndarray:
+    s = np.ascontiguousarray(s, dtype=np.float32)
+    out = np.empty_like(s)
+    lib().oracle_ue8m0_ceil_n(_p(s), _p(out), s.size)
+    return out
+
+
+def silu_mul(a, b) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    b = np.ascontiguousarray(b, dtype=np.float32)
+    out = np.empty_like(a)
+    lib().oracle_silu_mul_n(_p(a), _p(b), _p(out), a.size)
+    return out
+
+
+def quant_pairs(v, s) -> np.ndarray:
+    """e4m3(RN32(v / s)) elementwise."""
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    s = np.ascontiguousarray(s, dtype=np.float32)
+    out = np.empty(v.shape, np.uint8)
+    lib().oracle_quant_pairs(_p(v), _p(s), _p(out), v.size)
+    return out
+
+
+def row_sumsq(z_bits) -> np.ndarray:
+    z = _u16(z_bits)
+    T, H = z.shape
+    out = np.empty(T, np.float32)
+    lib().oracle_row_sumsq(_p(z), T, H, _p(out))
+    return out
+
+
+def rms_inv(ss: float, H: int, eps=RMS_EPS) -> np.float32:
+    return np.float32(lib().oracle_rms_inv(float(ss), int(H), float(eps)))
