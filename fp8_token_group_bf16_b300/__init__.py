@@ -1,1 +1,234 @@
-"""fp8_token_group_bf16_b300: fused FP8 per-group quantisation epilogues for B300 (sm_103a)."""
+"""fp8_token_group_bf16_b300: fused FP8 per-group quantisation epilogues for B300 (sm_103a).
+
+The compute lives in ``libfp8q.so`` (hand-written CUDA for sm_103a, C ABI in
+``include/fp8q.h``).  This package is a thin ctypes binding over it:
+
+* ``fp8q_per_token_group_quant``, ``fp8q_rms_norm_per_block_quant``,
+  ``fp8q_silu_and_mul_per_block_quant``, ``fp8q_f32_to_e4m3``,
+  ``fp8q_status_string`` -- the C entry points under their own names, taking
+  raw device pointers (ints) and sizes, returning the status code;
+* ``per_token_group_fp8_quant``, ``rms_norm_per_block_quant``,
+  ``silu_and_mul_per_block_quant`` -- the same calls on torch tensors:
+  argument checks, output allocation, the current CUDA stream, and an
+  exception on a non-zero status.  Every step of the computation runs in the
+  library's kernels; there is no CPU fallback.  If the library is missing or
+  no CUDA device is present the calls raise.
+
+The library is built in place by ``python -m fp8_token_group_bf16_b300.build``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG_DIR, "libfp8q.so")
+
+FP8Q_OK = 0
+FP8Q_ERR_INVALID_ARG = 1
+FP8Q_ERR_UNSUPPORTED = 2
+FP8Q_ERR_MISALIGNED = 3
+FP8Q_ERR_CUDA = 4
+FP8Q_SCALES_ROW_MAJOR = 0
+FP8Q_SCALES_COL_MAJOR = 1
+FP8Q_RMS_MAX_H = 65536
+GROUP = 128
+
+EXPORTS = (
+    "fp8q_per_token_group_quant",
+    "fp8q_rms_norm_per_block_quant",
+    "fp8q_silu_and_mul_per_block_quant",
+    "fp8q_f32_to_e4m3",
+    "fp8q_status_string",
+    "fp8q_version",
+)
+
+_lib = None
+
+
+class Fp8qError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {fp8q_status_string(status)} (status {status})")
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libfp8q.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(
+            f"libfp8q.so not found at {path}; build it with "
+            "`python -m fp8_token_group_bf16_b300.build` (needs nvcc)")
+    L = ctypes.CDLL(path)
+    P, I64, I32, F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+    L.fp8q_per_token_group_quant.argtypes = [P, P, P, I64, I64, I32, F, I32, I32, P]
+    L.fp8q_rms_norm_per_block_quant.argtypes = [P, P, P, P, P, I64, I64, I32, F, I32, I32, P]
+    L.fp8q_silu_and_mul_per_block_quant.argtypes = [P, P, P, I64, I64, I32, F, I32, I32, P]
+    L.fp8q_f32_to_e4m3.argtypes = [P, P, I64, P]
+    for n in EXPORTS[:4]:
+        getattr(L, n).restype = ctypes.c_int
+    L.fp8q_status_string.argtypes = [ctypes.c_int]
+    L.fp8q_status_string.restype = ctypes.c_char_p
+    L.fp8q_version.argtypes = []
+    L.fp8q_version.restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+# ----------------------------------------------- raw C entry points -----
+
+
+def fp8q_per_token_group_quant(x, q, scales, T, H, group_size, eps, ue8m0, scale_layout, stream):
+    return load().fp8q_per_token_group_quant(x, q, scales, T, H, group_size, eps, ue8m0,
+                                             scale_layout, stream)
+
+
+def fp8q_rms_norm_per_block_quant(x, residual, weight, q, scales, T, H, group_size, eps, ue8m0,
+                                  scale_layout, stream):
+    return load().fp8q_rms_norm_per_block_quant(x, residual, weight, q, scales, T, H, group_size,
+                                                eps, ue8m0, scale_layout, stream)
+
+
+def fp8q_silu_and_mul_per_block_quant(x, q, scales, T, I, group_size, eps, ue8m0, scale_layout,
+                                      stream):
+    return load().fp8q_silu_and_mul_per_block_quant(x, q, scales, T, I, group_size, eps, ue8m0,
+                                                    scale_layout, stream)
+
+
+def fp8q_f32_to_e4m3(v, out, n, stream):
+    return load().fp8q_f32_to_e4m3(v, out, n, stream)
+
+
+def fp8q_status_string(status: int) -> str:
+    return load().fp8q_status_string(int(status)).decode()
+
+
+def fp8q_version() -> int:
+    return load().fp8q_version()
+
+
+# ------------------------------------------------ tensor-level calls ----
+
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def _check(status: int, where: str):
+    if status != FP8Q_OK:
+        raise Fp8qError(status, where)
+
+
+def _stream_ptr(t, stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(t.device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _need_cuda_bf16(name, t):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if t.dtype != torch.bfloat16:
+        raise ValueError(f"{name} must be bfloat16, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _outputs(x, T, cols, group_size, column_major_scales, q, scales):
+    torch = _torch()
+    G = cols // group_size
+    if q is None:
+        q = torch.empty((T, cols), dtype=torch.float8_e4m3fn, device=x.device)
+    if scales is None:
+        if column_major_scales:
+            scales = torch.empty((G, T), dtype=torch.float32, device=x.device).t()
+        else:
+            scales = torch.empty((T, G), dtype=torch.float32, device=x.device)
+    return q, scales
+
+
+def _scale_ptr(scales, T, G, column_major_scales):
+    want = (1, T) if column_major_scales else (G, 1)
+    if tuple(scales.shape) != (T, G) or (T > 1 and G > 1 and tuple(scales.stride()) != want):
+        raise ValueError(f"scales must be a [T, G] = [{T}, {G}] fp32 tensor with strides {want}")
+    return scales.data_ptr()
+
+
+def per_token_group_fp8_quant(x, group_size: int = GROUP, eps: float = 1e-10, ue8m0: bool = False,
+                              column_major_scales: bool = False, q=None, scales=None, stream=None):
+    """x bf16 [T, H] (CUDA, contiguous) -> (q float8_e4m3fn [T, H], scales fp32 [T, H/g]).
+
+    Column-major scales come back as a [T, G] view of a [G, T] buffer."""
+    _need_cuda_bf16("x", x)
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D [T, H]")
+    T, H = x.shape
+    q, scales = _outputs(x, T, H, group_size, column_major_scales, q, scales)
+    sp = _scale_ptr(scales, T, H // max(group_size, 1), column_major_scales)
+    _check(fp8q_per_token_group_quant(
+        x.data_ptr(), q.data_ptr(), sp, T, H, group_size, eps, int(ue8m0),
+        FP8Q_SCALES_COL_MAJOR if column_major_scales else FP8Q_SCALES_ROW_MAJOR,
+        _stream_ptr(x, stream)), "per_token_group_fp8_quant")
+    return q, scales
+
+
+def rms_norm_per_block_quant(x, weight, residual=None, eps: float = 1e-6, group_size: int = GROUP,
+                             ue8m0: bool = False, column_major_scales: bool = False, q=None,
+                             scales=None, stream=None):
+    """RMSNorm(x [+ residual]) * weight, then group FP8 quantisation.
+
+    When ``residual`` is given it is updated in place to bf16(x + residual),
+    the value that is normalised.  Returns (q, scales)."""
+    _need_cuda_bf16("x", x)
+    _need_cuda_bf16("weight", weight)
+    if residual is not None:
+        _need_cuda_bf16("residual", residual)
+        if residual.shape != x.shape:
+            raise ValueError("residual must have the shape of x")
+    if x.dim() != 2 or weight.dim() != 1 or weight.shape[0] != x.shape[1]:
+        raise ValueError("x must be [T, H] and weight [H]")
+    T, H = x.shape
+    q, scales = _outputs(x, T, H, group_size, column_major_scales, q, scales)
+    sp = _scale_ptr(scales, T, H // max(group_size, 1), column_major_scales)
+    _check(fp8q_rms_norm_per_block_quant(
+        x.data_ptr(), residual.data_ptr() if residual is not None else None, weight.data_ptr(),
+        q.data_ptr(), sp, T, H, group_size, eps, int(ue8m0),
+        FP8Q_SCALES_COL_MAJOR if column_major_scales else FP8Q_SCALES_ROW_MAJOR,
+        _stream_ptr(x, stream)), "rms_norm_per_block_quant")
+    return q, scales
+
+
+def silu_and_mul_per_block_quant(x, group_size: int = GROUP, eps: float = 1e-10, ue8m0: bool = False,
+                                 column_major_scales: bool = False, q=None, scales=None,
+                                 stream=None):
+    """x bf16 [T, 2I] = [gate | up] -> quant(silu(gate) * up): (q [T, I], scales [T, I/g])."""
+    _need_cuda_bf16("x", x)
+    if x.dim() != 2 or x.shape[1] % 2:
+        raise ValueError("x must be [T, 2I]")
+    T, I = x.shape[0], x.shape[1] // 2
+    q, scales = _outputs(x, T, I, group_size, column_major_scales, q, scales)
+    sp = _scale_ptr(scales, T, I // max(group_size, 1), column_major_scales)
+    _check(fp8q_silu_and_mul_per_block_quant(
+        x.data_ptr(), q.data_ptr(), sp, T, I, group_size, eps, int(ue8m0),
+        FP8Q_SCALES_COL_MAJOR if column_major_scales else FP8Q_SCALES_ROW_MAJOR,
+        _stream_ptr(x, stream)), "silu_and_mul_per_block_quant")
+    return q, scales
+
+
+def f32_to_e4m3(v, out=None, stream=None):
+    """fp32 CUDA tensor -> float8_e4m3fn codes (round to nearest even, saturating)."""
+    torch = _torch()
+    if v.device.type != "cuda" or v.dtype != torch.float32 or not v.is_contiguous():
+        raise ValueError("v must be a contiguous fp32 CUDA tensor")
+    if out is None:
+        out = torch.empty(v.shape, dtype=torch.uint8, device=v.device)
+    _check(fp8q_f32_to_e4m3(v.data_ptr(), out.data_ptr(), v.numel(), _stream_ptr(v, stream)),
+           "f32_to_e4m3")
+    return out

@@ -1,0 +1,140 @@
+/*
+ * libfp8q — fused FP8 per-group quantisation epilogues for NVIDIA B300 (sm_103a).
+ *
+ * The three operations are the FP8 activation-quantisation custom ops of FP8
+ * LLM inference named in "[RFC]: Using Helion for Selected vLLM CustomOps"
+ * (Motivation, the list of kernels in the initial rollout):
+ * per_token_group_fp8_quant, silu_and_mul_per_block_quant and
+ * rms_norm_per_block_quant.  Their scale granularity is the Block_FP8
+ * "1x128 activation scaling" of "Helion：用自动调优改进 vLLM 推理" (section
+ * Scope): one fp32 scale per contiguous group of 128 values of a token row.
+ * The power-of-two scale option is the "float32 ceiling E8M0" scale format of
+ * the RFC's H100 end-to-end settings (also "UE8M0" in "Helion-Kernel in vLLM:
+ * PyTorch FP8 ohne CUDA", section "Praktische Einschränkungen").
+ *
+ * Arithmetic of every op, per group of 128 values v_i (fp32):
+ *   amax = max |v_i|;  s = RN32(max(amax, eps) / 448)
+ *   ue8m0 != 0:  s <- smallest power of two >= s (exact)
+ *   q_i  = e4m3fn(RN32(v_i / s)): round to nearest even, |.| > 448 -> +-448,
+ *          subnormals kept, sign of zero kept.
+ * The pages print no formula; this is the plain reading, and the library
+ * reproduces it bit for bit for per_token_group_quant.
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers are DEVICE pointers (global memory of the current device).  The
+ *    caller owns and allocates every buffer; the library allocates nothing
+ *    and keeps no state between calls.
+ *  - bf16 tensors are row-major and contiguous (row stride = row length);
+ *    `q` is float8_e4m3fn bytes, row-major [T, H] (or [T, I]).
+ *  - `x`, `q`, `residual` and `weight` must be 16-byte aligned, `scales`
+ *    4-byte aligned.  `q` must not alias `x`; `residual` must not alias `x`.
+ *  - Scale layout: FP8Q_SCALES_ROW_MAJOR stores s[t*G + g];
+ *    FP8Q_SCALES_COL_MAJOR stores s[g*T + t], G = H / group_size.
+ *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
+ *    stream.  Calls only enqueue work and never synchronise, so they can be
+ *    captured into CUDA graphs.
+ *  - Return value: an fp8q_status.  Invalid arguments are rejected before
+ *    anything is enqueued.  FP8Q_ERR_CUDA reports a failed launch
+ *    (cudaGetLastError after the launch); a fault while the kernel runs is
+ *    reported by CUDA at the caller's next synchronisation.  T == 0 returns
+ *    FP8Q_OK without a launch.  Calls never abort or throw.
+ */
+#ifndef FP8Q_H
+#define FP8Q_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FP8Q_API __attribute__((visibility("default")))
+#else
+#define FP8Q_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8Q_OK = 0,
+    FP8Q_ERR_INVALID_ARG = 1, /* negative T, H <= 0, H % group_size, NULL pointer, bad enum, bad eps */
+    FP8Q_ERR_UNSUPPORTED = 2, /* group_size != 128, or a row longer than the kernels handle */
+    FP8Q_ERR_MISALIGNED = 3,  /* a pointer below its required alignment */
+    FP8Q_ERR_CUDA = 4         /* the CUDA launch failed */
+} fp8q_status;
+
+typedef enum {
+    FP8Q_SCALES_ROW_MAJOR = 0, /* s[t*G + g] */
+    FP8Q_SCALES_COL_MAJOR = 1  /* s[g*T + t] */
+} fp8q_scale_layout;
+
+/* Longest rms_norm_per_block_quant row (H) the kernels accept. */
+#define FP8Q_RMS_MAX_H 65536
+
+/*
+ * per_token_group_fp8_quant.
+ *   x       bf16 [T, H], read.
+ *   q       e4m3 [T, H], written.
+ *   scales  fp32 [T*G] in `scale_layout`, written.
+ *   eps     floor of amax before the division by 448 (1e-10 in the reading
+ *           above); must be finite and >= 1e-30 so that every scale is a
+ *           normal fp32 number.
+ * Result: bit-identical to the arithmetic in the header comment.
+ */
+FP8Q_API int fp8q_per_token_group_quant(const void *x, void *q, float *scales, int64_t T, int64_t H,
+                               int32_t group_size, float eps, int32_t ue8m0, int32_t scale_layout,
+                               void *stream);
+
+/*
+ * rms_norm_per_block_quant: RMSNorm of each token row, then the group
+ * quantisation of the normalised row ("[RFC]: Using Helion for Selected vLLM
+ * CustomOps", Motivation; the routed op keeps the "schema and mutation
+ * contract" of the native op, section Routed Custom Op).
+ *   x         bf16 [T, H], read.
+ *   residual  bf16 [T, H] or NULL.  When given: z = bf16_RNE(x + residual) is
+ *             written back into `residual` (the mutation), and z is normalised.
+ *             Otherwise z = x.
+ *   weight    bf16 [H], read.
+ *   q, scales as for per_token_group_quant (scale floor 1e-10).
+ *   eps       the RMSNorm variance epsilon (e.g. 1e-6), finite and >= 0.
+ * Per row: ss = sum z_h^2 (fp32, tree order); inv = RN32(1/RN32(sqrt(
+ * RN32(RN32(ss/H) + eps)))); v_h = RN32(RN32(z_h * inv) * w_h); then the
+ * group quantisation of v.  Only the summation order of ss differs from a
+ * sequential sum, so scales agree with it to a few ulps and codes to one
+ * e4m3 step on rare elements.  H <= FP8Q_RMS_MAX_H.
+ */
+FP8Q_API int fp8q_rms_norm_per_block_quant(const void *x, void *residual, const void *weight, void *q,
+                                  float *scales, int64_t T, int64_t H, int32_t group_size,
+                                  float eps, int32_t ue8m0, int32_t scale_layout, void *stream);
+
+/*
+ * silu_and_mul_per_block_quant: SiLU(gate) * up, then the group quantisation
+ * ("[RFC]: Using Helion for Selected vLLM CustomOps", Motivation).
+ *   x       bf16 [T, 2I], read: gate a = x[t, 0:I], up b = x[t, I:2I].
+ *   q       e4m3 [T, I], written.
+ *   scales  fp32 [T*I/group_size] in `scale_layout`, written.
+ *   eps     amax floor, as for per_token_group_quant.
+ * v = RN32(RN32(a / RN32(1 + expf(-a))) * b) with CUDA's expf (within 2 ulp
+ * of exp), then the group quantisation of v.
+ */
+FP8Q_API int fp8q_silu_and_mul_per_block_quant(const void *x, void *q, float *scales, int64_t T, int64_t I,
+                                      int32_t group_size, float eps, int32_t ue8m0,
+                                      int32_t scale_layout, void *stream);
+
+/*
+ * Elementwise fp32 -> float8_e4m3fn with round to nearest even and
+ * saturation to +-448 (the rounding every op above applies to its
+ * quotients).  v: fp32 [n] read, out: e4m3 [n] written; both 16-byte
+ * aligned.  Exposed so the rounding can be checked on its own.
+ */
+FP8Q_API int fp8q_f32_to_e4m3(const float *v, void *out, int64_t n, void *stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+FP8Q_API const char *fp8q_status_string(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+FP8Q_API int fp8q_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FP8Q_H */

@@ -95,8 +95,8 @@ def _configure(L: ctypes.CDLL) -> ctypes.CDLL:
     F = ctypes.c_float
     I = ctypes.c_int
     L.oracle_per_token_group_quant.argtypes = [P, P, P, P, I64, I64, I64, F, I, I]
-    L.oracle_rms_norm_per_block_quant.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, F, I, I]
-    L.oracle_silu_and_mul_per_block_quant.argtypes = [P, P, P, P, I64, I64, I64, F, I, I]
+    L.oracle_rms_norm_per_block_quant.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I64, F, I, I]
+    L.oracle_silu_and_mul_per_block_quant.argtypes = [P, P, P, P, P, I64, I64, I64, F, I, I]
     for name in ("oracle_per_token_group_quant", "oracle_rms_norm_per_block_quant",
                  "oracle_silu_and_mul_per_block_quant"):
         getattr(L, name).restype = I
@@ -146,8 +146,9 @@ def per_token_group_quant(x_bits, group=128, eps=SCALE_EPS, ue8m0=False, col_maj
 
 
 def rms_norm_per_block_quant(x_bits, w_bits, residual_bits=None, group=128, eps=RMS_EPS,
-                             ue8m0=False, col_major=False):
-    """op B.  Returns (q, scales, scales_pre, inv [T], residual_out or None)."""
+                             ue8m0=False, col_major=False, want_values=False):
+    """op B.  Returns (q, scales, scales_pre, inv [T], residual_out or None),
+    plus the quantised fp32 values [T,H] when want_values."""
     x = _u16(x_bits)
     w = _u16(w_bits)
     T, H = x.shape
@@ -156,17 +157,22 @@ def rms_norm_per_block_quant(x_bits, w_bits, residual_bits=None, group=128, eps=
     s = np.empty(_scale_shape(T, G, col_major), np.float32)
     sp = np.empty_like(s)
     inv = np.empty(T, np.float32)
+    v = np.empty((T, H), np.float32) if want_values else None
     r = None
     if residual_bits is not None:
         r = np.array(_u16(residual_bits), copy=True)
     _check(lib().oracle_rms_norm_per_block_quant(
         _p(x), _p(r) if r is not None else None, _p(w), _p(q), _p(s), _p(sp), _p(inv),
-        T, H, group, float(eps), int(ue8m0), int(col_major)))
+        _p(v) if v is not None else None, T, H, group, float(eps), int(ue8m0), int(col_major)))
+    if want_values:
+        return q, s, sp, inv, r, v
     return q, s, sp, inv, r
 
 
-def silu_and_mul_per_block_quant(x_bits, group=128, eps=SCALE_EPS, ue8m0=False, col_major=False):
-    """op C.  x_bits uint16 [T, 2I].  Returns (q uint8 [T,I], scales, scales_pre)."""
+def silu_and_mul_per_block_quant(x_bits, group=128, eps=SCALE_EPS, ue8m0=False, col_major=False,
+                                 want_values=False):
+    """op C.  x_bits uint16 [T, 2I].  Returns (q uint8 [T,I], scales, scales_pre),
+    plus the quantised fp32 values [T,I] when want_values."""
     x = _u16(x_bits)
     T, H2 = x.shape
     I = H2 // 2
@@ -174,8 +180,12 @@ def silu_and_mul_per_block_quant(x_bits, group=128, eps=SCALE_EPS, ue8m0=False, 
     q = np.empty((T, I), np.uint8)
     s = np.empty(_scale_shape(T, G, col_major), np.float32)
     sp = np.empty_like(s)
-    _check(lib().oracle_silu_and_mul_per_block_quant(_p(x), _p(q), _p(s), _p(sp), T, I, group,
+    v = np.empty((T, I), np.float32) if want_values else None
+    _check(lib().oracle_silu_and_mul_per_block_quant(_p(x), _p(q), _p(s), _p(sp),
+                                                     _p(v) if v is not None else None, T, I, group,
                                                      float(eps), int(ue8m0), int(col_major)))
+    if want_values:
+        return q, s, sp, v
     return q, s, sp
 
 

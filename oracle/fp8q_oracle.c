@@ -239,8 +239,8 @@ float oracle_rms_inv(float ss, int64_t H, float eps)
 
 int oracle_rms_norm_per_block_quant(const uint16_t *x, uint16_t *residual, const uint16_t *w,
                                     uint8_t *q, float *scales, float *scales_pre, float *inv_out,
-                                    int64_t T, int64_t H, int64_t gs, float eps, int ue8m0,
-                                    int col_major)
+                                    float *v_out, int64_t T, int64_t H, int64_t gs, float eps,
+                                    int ue8m0, int col_major)
 {
     int rc = check_shape(T, H, gs);
     if (rc)
@@ -276,6 +276,8 @@ int oracle_rms_norm_per_block_quant(const uint16_t *x, uint16_t *residual, const
         for (int64_t h = 0; h < H; ++h) {
             float n = z[h] * inv;
             v[h] = n * oracle_bf16_to_f32(w[h]);
+            if (v_out)
+                v_out[t * H + h] = v[h];
         }
         for (int64_t g = 0; g < G; ++g) {
             float pre;
@@ -300,8 +302,8 @@ float oracle_silu_mul(float a, float b)
 }
 
 int oracle_silu_and_mul_per_block_quant(const uint16_t *x, uint8_t *q, float *scales,
-                                        float *scales_pre, int64_t T, int64_t I, int64_t gs,
-                                        float eps, int ue8m0, int col_major)
+                                        float *scales_pre, float *v_out, int64_t T, int64_t I,
+                                        int64_t gs, float eps, int ue8m0, int col_major)
 {
     int rc = check_shape(T, I, gs);
     if (rc)
@@ -317,6 +319,8 @@ int oracle_silu_and_mul_per_block_quant(const uint16_t *x, uint8_t *q, float *sc
                 float a = oracle_bf16_to_f32(xr[g * gs + i]);
                 float b = oracle_bf16_to_f32(xr[I + g * gs + i]);
                 v[i] = oracle_silu_mul(a, b);
+                if (v_out)
+                    v_out[t * I + g * gs + i] = v[i];
             }
             float pre;
             float s = oracle_group_scale(group_amax(v, gs), eps, ue8m0, &pre);

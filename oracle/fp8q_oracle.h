@@ -42,16 +42,18 @@ int oracle_per_token_group_quant(const uint16_t *x, uint8_t *q, float *scales, f
 
 /* op B: x bf16 [T,H], residual bf16 [T,H] in/out or NULL, w bf16 [H];
  * eps is the RMSNorm variance epsilon; the scale floor is ORACLE_SCALE_EPS.
- * inv_out (may be NULL) receives each row's 1/rms. */
+ * inv_out (may be NULL) receives each row's 1/rms; v_out (may be NULL) the
+ * fp32 values [T,H] that are quantised. */
 int oracle_rms_norm_per_block_quant(const uint16_t *x, uint16_t *residual, const uint16_t *w,
                                     uint8_t *q, float *scales, float *scales_pre, float *inv_out,
-                                    int64_t T, int64_t H, int64_t gs, float eps, int ue8m0,
-                                    int col_major);
+                                    float *v_out, int64_t T, int64_t H, int64_t gs, float eps,
+                                    int ue8m0, int col_major);
 
-/* op C: x bf16 [T,2I] (gate | up) -> q e4m3 [T,I], scales fp32 [T*I/gs] */
+/* op C: x bf16 [T,2I] (gate | up) -> q e4m3 [T,I], scales fp32 [T*I/gs];
+ * v_out (may be NULL) receives the fp32 values [T,I] that are quantised. */
 int oracle_silu_and_mul_per_block_quant(const uint16_t *x, uint8_t *q, float *scales,
-                                        float *scales_pre, int64_t T, int64_t I, int64_t gs,
-                                        float eps, int ue8m0, int col_major);
+                                        float *scales_pre, float *v_out, int64_t T, int64_t I,
+                                        int64_t gs, float eps, int ue8m0, int col_major);
 
 void oracle_f32_to_e4m3_n(const float *v, uint8_t *out, int64_t n);
 void oracle_ue8m0_ceil_n(const float *s, float *out, int64_t n);

@@ -1,0 +1,276 @@
+"""Parity of the CUDA library with the CPU oracle, through the C ABI.
+
+per_token_group_fp8_quant is compared bit for bit; the fused ops with the
+rules of tolerance.py.  Inputs are the seeded workloads of
+fp8_token_group_bf16_b300.inputs; tensors too large for the oracle are
+compared on sampled rows (rows are independent, so the oracle run on those
+rows alone gives their exact expected values), in the same launch
+configuration the benchmark times.
+"""
+
+import functools
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import pins
+from fp8_token_group_bf16_b300 import inputs
+from gpu_util import gpu_group_quant, gpu_rms, gpu_silu, require_gpu, sample_rows
+from tolerance import assert_exact, check_fused, to_tg
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = [(u, c) for u in (False, True) for c in (False, True)]
+VID = [f"{'ue8m0' if u else 'fp32'}-{'col' if c else 'row'}" for u, c in VARIANTS]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+@functools.lru_cache(maxsize=2)
+def _heavy_bits(T):
+    return inputs.bits(inputs.heavy_tailed_input(T, inputs.SWEEP_H, inputs.sweep_seed(T)))
+
+
+# ------------------------------------------------------- op A (exact) ----
+
+
+def _oracle_a(xb, ue8m0):
+    q, s, _ = oracle.per_token_group_quant(xb, ue8m0=ue8m0, col_major=False)
+    return q, s
+
+
+@pytest.mark.parametrize("ue8m0,col", VARIANTS, ids=VID)
+def test_group_quant_small_case_with_hand_rows(ue8m0, col):
+    xb = inputs.bits(inputs.small_group_quant_input())
+    q, s = gpu_group_quant(xb, ue8m0, col)
+    qr, sr, _ = oracle.per_token_group_quant(xb, ue8m0=ue8m0, col_major=col)
+    assert_exact(q, s, qr, to_tg(sr, col), "small case")
+    # the hand-derived midpoint codes, straight from the golden file
+    golden = [c for _, c in pins.load_midpoints()][:-2]
+    assert q[18, : len(golden)].tolist() == golden
+
+
+@pytest.mark.parametrize("ue8m0,col", VARIANTS, ids=VID)
+@pytest.mark.parametrize("T", inputs.SWEEP_T)
+def test_group_quant_heavy_tailed_sweep(T, ue8m0, col):
+    xb = _heavy_bits(T)
+    q, s = gpu_group_quant(xb, ue8m0, col)
+    rows = sample_rows(T, 512, seed=T)
+    qr, sr = _oracle_a(np.ascontiguousarray(xb[rows]), ue8m0)
+    assert_exact(q[rows], s[rows], qr, sr, f"T={T}")
+
+
+def test_group_quant_near_midpoint_quotients():
+    xb = pins.near_midpoint_groups(pins.near_midpoint_cases(n_scales=3000, seed=9))
+    for ue8m0 in (False, True):
+        q, s = gpu_group_quant(xb, ue8m0)
+        qr, sr = _oracle_a(xb, ue8m0)
+        assert_exact(q, s, qr, sr, f"near midpoints ue8m0={ue8m0}")
+
+
+def _quotient_domain_groups(stride: int) -> np.ndarray:
+    """Groups [amax, x_1 .. x_127] for every stride-th positive finite bf16
+    amax and every bf16 x with |x| <= amax (alternating signs): the whole
+    domain of the quotient x / RN32(amax/448) that the op can meet."""
+    b = pins.all_bf16_finite()
+    pos = b[(b >> 15) == 0]
+    vals = pins.bf16_bits_to_f32(pos)
+    order = np.argsort(vals, kind="stable")
+    pos, vals = pos[order], vals[order]
+    groups = []
+    for i in range(1, len(pos), stride):
+        xs = pos[: i + 1]
+        xs = np.where(np.arange(xs.size) % 2 == 1, xs | np.uint16(0x8000), xs).astype(np.uint16)
+        n = -(-xs.size // 127)
+        padded = np.resize(xs, n * 127).reshape(n, 127)
+        g = np.empty((n, 128), np.uint16)
+        g[:, 0] = pos[i]
+        g[:, 1:] = padded
+        groups.append(g)
+    allg = np.concatenate(groups)
+    pad = (-allg.shape[0]) % 8
+    if pad:
+        allg = np.concatenate([allg, allg[:pad]])
+    return allg.reshape(-1, 8 * 128)
+
+
+def test_group_quant_quotient_domain():
+    stride = 1 if os.environ.get("FP8Q_EXHAUSTIVE") else 61
+    xb = _quotient_domain_groups(stride)
+    for ue8m0 in (False, True):
+        q, s = gpu_group_quant(xb, ue8m0)
+        qr, sr = _oracle_a(xb, ue8m0)
+        assert_exact(q, s, qr, sr, f"quotient domain ue8m0={ue8m0}")
+
+
+@pytest.mark.parametrize("T,H", [(1, 128), (2, 256), (3, 384), (5, 640), (37, 7168), (1000, 128),
+                                 (7, 1152), (129, 896), (4097, 256)])
+@pytest.mark.parametrize("ue8m0,col", VARIANTS, ids=VID)
+def test_group_quant_ragged_shapes(T, H, ue8m0, col):
+    xb = inputs.bits(inputs.heavy_tailed_input(T, H, seed=77 + T + H))
+    q, s = gpu_group_quant(xb, ue8m0, col)
+    qr, sr = _oracle_a(xb, ue8m0)
+    assert_exact(q, s, qr, sr, f"T={T} H={H}")
+
+
+# ------------------------------------------- e4m3 conversion on its own --
+
+
+def test_f32_to_e4m3_conversion():
+    import fp8_token_group_bf16_b300 as fq
+
+    rng = np.random.default_rng(1)
+    v = np.concatenate([
+        pins.bf16_bits_to_f32(pins.all_bf16_finite()),
+        pins.structured_f32(),
+        rng.integers(0, 2**32, size=1 << 24, dtype=np.uint64).astype(np.uint32).view(np.float32),
+    ])
+    v = v[~np.isnan(v)]
+    got = fq.f32_to_e4m3(torch.from_numpy(v).cuda()).cpu().numpy()
+    want = oracle.f32_to_e4m3(v)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, (bad.size, v[bad[:4]], got[bad[:4]], want[bad[:4]])
+
+
+def test_f32_to_e4m3_all_fp32_patterns():
+    """Every non-NaN fp32 bit pattern (2^32) when FP8Q_EXHAUSTIVE is set,
+    otherwise every 61st pattern."""
+    import fp8_token_group_bf16_b300 as fq
+
+    step = 1 if os.environ.get("FP8Q_EXHAUSTIVE") else 61
+    chunk = 1 << 26
+    for start in range(0, 1 << 32, chunk * step):
+        u = np.arange(start, min(start + chunk * step, 1 << 32), step, dtype=np.uint64).astype(np.uint32)
+        v = u.view(np.float32)
+        v = v[~np.isnan(v)]
+        got = fq.f32_to_e4m3(torch.from_numpy(v).cuda()).cpu().numpy()
+        want = oracle.f32_to_e4m3(v)
+        bad = np.nonzero(got != want)[0]
+        assert bad.size == 0, (start, bad.size, v[bad[:4]], got[bad[:4]], want[bad[:4]])
+
+
+# ----------------------------------------------- op B (rms + quant) ----
+
+
+def _check_rms(xb, wb, rb, ue8m0, col, rows=None, what=""):
+    q, s, rout = gpu_rms(xb, wb, rb, ue8m0, col)
+    if rows is None:
+        rows = np.arange(xb.shape[0])
+    xs = np.ascontiguousarray(xb[rows])
+    rs = np.ascontiguousarray(rb[rows]) if rb is not None else None
+    qr, sr, spr, _, ror, vr = oracle.rms_norm_per_block_quant(xs, wb, rs, ue8m0=ue8m0, want_values=True)
+    if rb is not None:
+        assert np.array_equal(rout[rows], ror), f"{what}: residual output differs"
+    return check_fused(q[rows], s[rows], qr, sr, spr, vr, ue8m0, what)
+
+
+@pytest.mark.parametrize("residual", [False, True], ids=["plain", "residual"])
+@pytest.mark.parametrize("ue8m0,col", VARIANTS, ids=VID)
+def test_rms_4096(residual, ue8m0, col):
+    x, w, r = inputs.rms_input(256, 4096)
+    _check_rms(inputs.bits(x), inputs.bits(w), inputs.bits(r) if residual else None, ue8m0, col,
+               what=f"rms 256x4096 residual={residual}")
+
+
+@pytest.mark.parametrize("T", inputs.MIX_T)
+def test_rms_qwen3_mix(T):
+    x = inputs.lognormal_channel_input(T, inputs.MIX_H, inputs.mix_seed(T))
+    w = inputs.rms_weight(inputs.MIX_H)
+    rows = sample_rows(T, 512, seed=T)
+    _check_rms(inputs.bits(x), inputs.bits(w), None, True, False, rows, what=f"rms mix T={T}")
+
+
+@pytest.mark.parametrize("T,H", [(1, 128), (3, 384), (37, 1152), (2, 8192), (5, 16384),
+                                 (3, 24576), (2, 65536), (300, 256)])
+@pytest.mark.parametrize("residual", [False, True], ids=["plain", "residual"])
+def test_rms_ragged_shapes(T, H, residual):
+    x, w, r = inputs.rms_input(T, H, seeds=(900 + T, 901 + H, 902))
+    for ue8m0, col in VARIANTS:
+        _check_rms(inputs.bits(x), inputs.bits(w), inputs.bits(r) if residual else None, ue8m0, col,
+                   what=f"rms T={T} H={H}")
+
+
+def test_rms_degenerate_rows():
+    """All-zero row (inv = 1/sqrt(eps), every value 0, floor scale) and a
+    constant row (every code +-448)."""
+    H = 1024
+    x = torch.zeros(4, H)
+    x[1] = 0.75
+    x[2] = -3.0
+    x[3, ::2] = 1e-20
+    xb = inputs.bits(inputs.bf16(x))
+    wb = inputs.bits(inputs.bf16(torch.ones(H)))
+    for ue8m0, col in VARIANTS:
+        q, s, _ = gpu_rms(xb, wb, None, ue8m0, col)
+        qr, sr, _, _, _ = oracle.rms_norm_per_block_quant(xb, wb, None, ue8m0=ue8m0)
+        assert_exact(q, s, qr, sr, "degenerate rows")
+
+
+# ---------------------------------------------- op C (silu + quant) ----
+
+
+def _check_silu(xb, ue8m0, col, rows=None, what=""):
+    q, s = gpu_silu(xb, ue8m0, col)
+    if rows is None:
+        rows = np.arange(xb.shape[0])
+    qr, sr, spr, vr = oracle.silu_and_mul_per_block_quant(np.ascontiguousarray(xb[rows]), ue8m0=ue8m0,
+                                                          want_values=True)
+    return check_fused(q[rows], s[rows], qr, sr, spr, vr, ue8m0, what)
+
+
+def test_silu_12288_ue8m0_col_major():
+    xb = inputs.bits(inputs.silu_input(1024, 12288))
+    _check_silu(xb, True, True, what="silu 1024x12288")
+
+
+@pytest.mark.parametrize("ue8m0,col", VARIANTS, ids=VID)
+def test_silu_12288_other_variants(ue8m0, col):
+    xb = inputs.bits(inputs.silu_input(64, 12288, seed=inputs.SEED_SILU + 1))
+    _check_silu(xb, ue8m0, col, what="silu 64x12288")
+
+
+@pytest.mark.parametrize("T", inputs.MIX_T)
+def test_silu_qwen3_mix(T):
+    x = inputs.lognormal_channel_input(T, 2 * inputs.MIX_I, inputs.mix_seed(T) + 50)
+    rows = sample_rows(T, 128, seed=T)
+    _check_silu(inputs.bits(x), True, False, rows, what=f"silu mix T={T}")
+
+
+def test_silu_reduces_to_group_quant():
+    """gate >= 20 and up = 1: silu(a) * 1 == a exactly, so the result must be
+    the per-group quantisation of the gate half, bit for bit."""
+    rng = np.random.default_rng(5)
+    T, I = 64, 7168
+    a = (20.0 + np.abs(rng.standard_normal((T, I))) * 40.0).astype(np.float32)
+    ab = inputs.bits(inputs.bf16(torch.from_numpy(a)))
+    xb = np.concatenate([ab, inputs.bits(inputs.bf16(torch.ones(T, I)))], axis=1)
+    for ue8m0, col in VARIANTS:
+        q, s = gpu_silu(xb, ue8m0, col)
+        qr, sr = _oracle_a(ab, ue8m0)
+        assert_exact(q, s, qr, sr, "silu reduction")
+
+
+@pytest.mark.parametrize("T,I", [(1, 128), (3, 384), (37, 1152), (5, 640), (1000, 256)])
+def test_silu_ragged_shapes(T, I):
+    xb = inputs.bits(inputs.silu_input(T, I, seed=700 + T + I))
+    for ue8m0, col in VARIANTS:
+        _check_silu(xb, ue8m0, col, what=f"silu T={T} I={I}")
+
+
+def test_silu_extreme_gates():
+    """Gates far below -88 (exp overflows, silu -> -0), zeros, and +-0 ups."""
+    T, I = 4, 256
+    a = torch.randn(T, I, generator=torch.Generator().manual_seed(3)) * 50.0
+    a[0] = -200.0
+    a[1, ::3] = 0.0
+    b = torch.randn(T, I, generator=torch.Generator().manual_seed(4))
+    b[2, ::2] = -0.0
+    xb = inputs.bits(inputs.bf16(torch.cat([a, b], dim=1)))
+    for ue8m0, col in VARIANTS:
+        _check_silu(xb, ue8m0, col, what="silu extreme gates")

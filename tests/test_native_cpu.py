@@ -1,0 +1,143 @@
+"""libfp8q on a machine without a GPU: it builds for sm_103a, loads, exports
+exactly the C ABI that include/fp8q.h declares, and rejects bad arguments on
+the host before touching CUDA.  No call here reaches a kernel launch."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import fp8_token_group_bf16_b300 as fq
+from fp8_token_group_bf16_b300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8q.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return fq.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp8q_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_three_ops():
+    names = declared_functions()
+    for n in ("fp8q_per_token_group_quant", "fp8q_rms_norm_per_block_quant",
+              "fp8q_silu_and_mul_per_block_quant", "fp8q_status_string"):
+        assert n in names
+
+
+def test_exports_match_header(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", fq.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = sorted({l.split()[-1] for l in out.splitlines() if " T " in l and l.split()[-1].startswith("fp8q_")})
+    assert exported == declared_functions()
+    for n in declared_functions():
+        assert hasattr(lib, n)
+    assert sorted(fq.EXPORTS) == declared_functions()
+
+
+def test_only_c_abi_symbols_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", fq.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    text_syms = [l.split()[-1] for l in out.splitlines() if " T " in l]
+    assert all(s.startswith("fp8q_") for s in text_syms), [s for s in text_syms if not s.startswith("fp8q_")][:5]
+
+
+def test_built_for_sm103a(lib):
+    out = subprocess.run(["cuobjdump", "--list-elf", fq.LIB_PATH], capture_output=True, text=True)
+    if out.returncode == 0:
+        assert "sm_103a" in out.stdout
+
+
+def test_status_strings(lib):
+    for s in range(5):
+        assert fq.fp8q_status_string(s).startswith("FP8Q_")
+    assert "unknown" in fq.fp8q_status_string(99)
+    assert fq.fp8q_version() >= 100
+
+
+# Fake, never-dereferenced device addresses: every call below is rejected by
+# the host-side checks before any CUDA call.
+A = 0x7F0000000000
+Q = 0x7F0000100000
+S = 0x7F0000200000
+
+
+def test_rejects_bad_shapes(lib):
+    E = fq.FP8Q_ERR_INVALID_ARG
+    assert fq.fp8q_per_token_group_quant(A, Q, S, -1, 512, 128, 1e-10, 0, 0, None) == E
+    assert fq.fp8q_per_token_group_quant(A, Q, S, 4, 0, 128, 1e-10, 0, 0, None) == E
+    assert fq.fp8q_per_token_group_quant(A, Q, S, 4, 500, 128, 1e-10, 0, 0, None) == E
+    assert fq.fp8q_per_token_group_quant(A, Q, S, 4, 512, 128, 1e-10, 0, 2, None) == E
+    assert fq.fp8q_per_token_group_quant(None, Q, S, 4, 512, 128, 1e-10, 0, 0, None) == E
+    assert fq.fp8q_silu_and_mul_per_block_quant(A, Q, S, 4, 100, 128, 1e-10, 0, 0, None) == E
+    assert fq.fp8q_rms_norm_per_block_quant(A, None, None, Q, S, 4, 512, 128, 1e-6, 0, 0, None) == E
+
+
+def test_rejects_bad_eps(lib):
+    E = fq.FP8Q_ERR_INVALID_ARG
+    for eps in (0.0, -1.0, float("inf"), float("nan"), 1e-38):
+        assert fq.fp8q_per_token_group_quant(A, Q, S, 4, 512, 128, eps, 0, 0, None) == E
+        assert fq.fp8q_silu_and_mul_per_block_quant(A, Q, S, 4, 512, 128, eps, 0, 0, None) == E
+    for eps in (-1e-6, float("inf"), float("nan")):
+        assert fq.fp8q_rms_norm_per_block_quant(A, None, A, Q, S, 4, 512, 128, eps, 0, 0, None) == E
+
+
+def test_unsupported(lib):
+    U = fq.FP8Q_ERR_UNSUPPORTED
+    assert fq.fp8q_per_token_group_quant(A, Q, S, 4, 512, 64, 1e-10, 0, 0, None) == U
+    assert fq.fp8q_rms_norm_per_block_quant(A, None, A, Q, S, 4, 512, 256, 1e-6, 0, 0, None) == U
+    assert fq.fp8q_rms_norm_per_block_quant(A, None, A, Q, S, 4, fq.FP8Q_RMS_MAX_H + 128, 128, 1e-6,
+                                            0, 0, None) == U
+
+
+def test_misaligned(lib):
+    M = fq.FP8Q_ERR_MISALIGNED
+    assert fq.fp8q_per_token_group_quant(A + 2, Q, S, 4, 512, 128, 1e-10, 0, 0, None) == M
+    assert fq.fp8q_per_token_group_quant(A, Q + 8, S, 4, 512, 128, 1e-10, 0, 0, None) == M
+    assert fq.fp8q_per_token_group_quant(A, Q, S + 2, 4, 512, 128, 1e-10, 0, 0, None) == M
+    assert fq.fp8q_silu_and_mul_per_block_quant(A + 4, Q, S, 4, 512, 128, 1e-10, 0, 0, None) == M
+    assert fq.fp8q_rms_norm_per_block_quant(A, A + 8, A, Q, S, 4, 512, 128, 1e-6, 0, 0, None) == M
+    assert fq.fp8q_rms_norm_per_block_quant(A, None, A + 2, Q, S, 4, 512, 128, 1e-6, 0, 0, None) == M
+    assert fq.fp8q_f32_to_e4m3(A + 4, Q, 16, None) == M
+
+
+def test_empty_input_is_a_no_op(lib):
+    # T == 0 returns before any CUDA call, even with null pointers.
+    assert fq.fp8q_per_token_group_quant(None, None, None, 0, 512, 128, 1e-10, 0, 0, None) == 0
+    assert fq.fp8q_silu_and_mul_per_block_quant(None, None, None, 0, 512, 128, 1e-10, 1, 1, None) == 0
+    assert fq.fp8q_rms_norm_per_block_quant(None, None, None, None, None, 0, 512, 128, 1e-6, 0, 0, None) == 0
+    assert fq.fp8q_f32_to_e4m3(None, None, 0, None) == 0
+
+
+def test_tensor_api_refuses_cpu_tensors(lib):
+    import torch
+
+    x = torch.zeros(4, 512, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        fq.per_token_group_fp8_quant(x)
+    with pytest.raises(ValueError, match="CUDA"):
+        fq.silu_and_mul_per_block_quant(x)
+    with pytest.raises(ValueError, match="CUDA"):
+        fq.rms_norm_per_block_quant(x, torch.ones(512, dtype=torch.bfloat16))
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    import importlib
+
+    saved = fq._lib
+    fq._lib = None
+    try:
+        with pytest.raises(ImportError, match="not found"):
+            fq.load(str(tmp_path / "libfp8q.so"))
+    finally:
+        fq._lib = saved
