@@ -11,9 +11,6 @@ namespace {
 
 using namespace fp8q;
 
-constexpr int kThreads = 256;           // op A / op C CTA size (16 half-warps)
-constexpr int kHalfWarpsPerCta = kThreads / kLanesPerGroup;
-
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int check_common(const void *x, const void *q, const float *scales, int64_t T, int64_t H,
@@ -34,65 +31,89 @@ int check_common(const void *x, const void *q, const float *scales, int64_t T, i
     return FP8Q_OK;
 }
 
+// T*G groups must fit the kernels' 32-bit group split (2^31 groups of 128
+// bf16 values would be 512 GiB of input, more than the device holds).
+int check_groups(int64_t T, int64_t G)
+{
+    const int64_t n = T * G;
+    if (n / T != G || n >= (int64_t(1) << 31))
+        return FP8Q_ERR_UNSUPPORTED;
+    return FP8Q_OK;
+}
+
 bool valid_scale_eps(float eps) { return std::isfinite(eps) && eps >= 1e-30f; }
 
-int launch_status()
+int launch_status(cudaError_t launched)
 {
-    return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
+    const cudaError_t last = cudaGetLastError();
+    return (launched == cudaSuccess && last == cudaSuccess) ? FP8Q_OK : FP8Q_ERR_CUDA;
 }
 
-// Groups per half-warp: more independent loads per thread for large inputs,
-// more CTAs (more SMs pulling) for small ones.
-int pick_gpt(int64_t n_groups)
+// Number of SMs of the current device (148 on B300); 1 if it cannot be read.
+int sm_count()
 {
-    const int64_t ctas_at_4 = (n_groups + 4 * kHalfWarpsPerCta - 1) / (4 * kHalfWarpsPerCta);
-    if (ctas_at_4 >= 4 * 148)
-        return 4;
-    const int64_t ctas_at_2 = (n_groups + 2 * kHalfWarpsPerCta - 1) / (2 * kHalfWarpsPerCta);
-    if (ctas_at_2 >= 2 * 148)
-        return 2;
-    return 1;
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return 1;
+    return n;
 }
 
-template <bool U, bool C>
-void launch_group(int gpt, const uint16_t *x, uint8_t *q, float *s, int64_t n, int64_t G,
-                  int64_t T, float eps, cudaStream_t st)
+// Launch with programmatic stream serialization allowed: the kernel may be
+// scheduled while its predecessor on the stream drains, and waits for it
+// (griddepcontrol.wait) before touching global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t st, Args... args)
 {
-    const int64_t per = int64_t(kHalfWarpsPerCta) * gpt;
-    const dim3 grid(unsigned((n + per - 1) / per));
-    switch (gpt) {
-    case 4: group_quant_kernel<U, C, 4><<<grid, kThreads, 0, st>>>(x, q, s, n, G, T, eps); break;
-    case 2: group_quant_kernel<U, C, 2><<<grid, kThreads, 0, st>>>(x, q, s, n, G, T, eps); break;
-    default: group_quant_kernel<U, C, 1><<<grid, kThreads, 0, st>>>(x, q, s, n, G, T, eps); break;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+#ifndef FP8Q_NO_PDL
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+#endif
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+template <bool U, bool C, bool V>
+cudaError_t launch_group(const uint16_t *x, uint8_t *q, float *s, int64_t n, int64_t G, int64_t T,
+                         float eps, cudaStream_t st)
+{
+    const int64_t per = int64_t(kGroupsPerCta) * kGroupQuantGpt;
+    return launch(group_quant_kernel<U, C, V>, dim3{unsigned((n + per - 1) / per)},
+                  dim3{unsigned(kCtaThreads)}, st, x, q, s, n, G, T, eps);
+}
+
+template <bool U, bool C, bool V>
+cudaError_t launch_silu(const uint16_t *x, uint8_t *q, float *s, int64_t n, int64_t G, int64_t T,
+                        int64_t I, float eps, cudaStream_t st)
+{
+    return launch(silu_quant_kernel<U, C, V>, dim3{unsigned((n + kGroupsPerCta - 1) / kGroupsPerCta)},
+                  dim3{unsigned(kCtaThreads)}, st, x, q, s, n, G, T, I, eps);
+}
+
+template <bool U, bool C, bool R, bool V, bool L>
+cudaError_t launch_rms(const uint16_t *x, uint16_t *res, const uint16_t *w, uint8_t *q, float *s,
+                       int64_t T, int H, int G, float eps, cudaStream_t st)
+{
+    const int threads = ((4 * G + 31) / 32) * 32;
+    int64_t grid = T;
+    if (!L) {
+        // persistent: as many CTAs as are resident at once, at most one per row
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rms_quant_kernel<U, C, R, V, L>,
+                                                          threads, 0) != cudaSuccess || per_sm < 1)
+            per_sm = 1;
+        const int64_t resident = int64_t(per_sm) * sm_count();
+        grid = T < resident ? T : resident;
     }
-}
-
-template <bool U, bool C>
-void launch_silu(int gpt, const uint16_t *x, uint8_t *q, float *s, int64_t n, int64_t G,
-                 int64_t T, int64_t I, float eps, cudaStream_t st)
-{
-    const int64_t per = int64_t(kHalfWarpsPerCta) * gpt;
-    const dim3 grid(unsigned((n + per - 1) / per));
-    switch (gpt) {
-    case 4: silu_quant_kernel<U, C, 4><<<grid, kThreads, 0, st>>>(x, q, s, n, G, T, I, eps); break;
-    case 2: silu_quant_kernel<U, C, 2><<<grid, kThreads, 0, st>>>(x, q, s, n, G, T, I, eps); break;
-    default: silu_quant_kernel<U, C, 1><<<grid, kThreads, 0, st>>>(x, q, s, n, G, T, I, eps); break;
-    }
-}
-
-template <bool U, bool C, bool R>
-void launch_rms(int P, const uint16_t *x, uint16_t *res, const uint16_t *w, uint8_t *q,
-                float *s, int64_t T, int H, int G, float eps, cudaStream_t st)
-{
-    const int warps = (G + 2 * P - 1) / (2 * P);
-    const dim3 grid{unsigned(T)};
-    const dim3 block{unsigned(32 * warps)};
-    switch (P) {
-    case 1: rms_quant_kernel<U, C, R, 1><<<grid, block, 0, st>>>(x, res, w, q, s, T, H, G, eps); break;
-    case 2: rms_quant_kernel<U, C, R, 2><<<grid, block, 0, st>>>(x, res, w, q, s, T, H, G, eps); break;
-    case 4: rms_quant_kernel<U, C, R, 4><<<grid, block, 0, st>>>(x, res, w, q, s, T, H, G, eps); break;
-    default: rms_quant_kernel<U, C, R, 8><<<grid, block, 0, st>>>(x, res, w, q, s, T, H, G, eps); break;
-    }
+    return launch(rms_quant_kernel<U, C, R, V, L>, dim3{unsigned(grid)}, dim3{unsigned(threads)}, st,
+                  x, res, w, q, s, T, H, G, eps);
 }
 
 }  // namespace
@@ -111,22 +132,24 @@ int fp8q_per_token_group_quant(const void *x, void *q, float *scales, int64_t T,
     if (T == 0)
         return FP8Q_OK;
     const int64_t G = H / kGroup;
+    if ((rc = check_groups(T, G)) != FP8Q_OK)
+        return rc;
     const int64_t n = T * G;
-    if (n / T != G || n > (int64_t(1) << 40))
-        return FP8Q_ERR_INVALID_ARG;
     auto st = static_cast<cudaStream_t>(stream);
     auto xp = static_cast<const uint16_t *>(x);
     auto qp = static_cast<uint8_t *>(q);
-    const int gpt = pick_gpt(n);
     const bool col = scale_layout == FP8Q_SCALES_COL_MAJOR;
-    if (ue8m0) {
-        if (col) launch_group<true, true>(gpt, xp, qp, scales, n, G, T, eps, st);
-        else     launch_group<true, false>(gpt, xp, qp, scales, n, G, T, eps, st);
-    } else {
-        if (col) launch_group<false, true>(gpt, xp, qp, scales, n, G, T, eps, st);
-        else     launch_group<false, false>(gpt, xp, qp, scales, n, G, T, eps, st);
-    }
-    return launch_status();
+    const bool v8 = aligned(x, 32) && aligned(q, 32);
+    cudaError_t e;
+#define FP8Q_GROUP(U, C)                                                                         \
+    (v8 ? launch_group<U, C, true>(xp, qp, scales, n, G, T, eps, st)                            \
+        : launch_group<U, C, false>(xp, qp, scales, n, G, T, eps, st))
+    if (ue8m0)
+        e = col ? FP8Q_GROUP(true, true) : FP8Q_GROUP(true, false);
+    else
+        e = col ? FP8Q_GROUP(false, true) : FP8Q_GROUP(false, false);
+#undef FP8Q_GROUP
+    return launch_status(e);
 }
 
 int fp8q_silu_and_mul_per_block_quant(const void *x, void *q, float *scales, int64_t T, int64_t I,
@@ -141,22 +164,24 @@ int fp8q_silu_and_mul_per_block_quant(const void *x, void *q, float *scales, int
     if (T == 0)
         return FP8Q_OK;
     const int64_t G = I / kGroup;
+    if ((rc = check_groups(T, G)) != FP8Q_OK)
+        return rc;
     const int64_t n = T * G;
-    if (n / T != G || n > (int64_t(1) << 40))
-        return FP8Q_ERR_INVALID_ARG;
     auto st = static_cast<cudaStream_t>(stream);
     auto xp = static_cast<const uint16_t *>(x);
     auto qp = static_cast<uint8_t *>(q);
-    const int gpt = pick_gpt(n);
     const bool col = scale_layout == FP8Q_SCALES_COL_MAJOR;
-    if (ue8m0) {
-        if (col) launch_silu<true, true>(gpt, xp, qp, scales, n, G, T, I, eps, st);
-        else     launch_silu<true, false>(gpt, xp, qp, scales, n, G, T, I, eps, st);
-    } else {
-        if (col) launch_silu<false, true>(gpt, xp, qp, scales, n, G, T, I, eps, st);
-        else     launch_silu<false, false>(gpt, xp, qp, scales, n, G, T, I, eps, st);
-    }
-    return launch_status();
+    const bool v8 = aligned(x, 32) && aligned(q, 32);
+    cudaError_t e;
+#define FP8Q_SILU(U, C)                                                                          \
+    (v8 ? launch_silu<U, C, true>(xp, qp, scales, n, G, T, I, eps, st)                          \
+        : launch_silu<U, C, false>(xp, qp, scales, n, G, T, I, eps, st))
+    if (ue8m0)
+        e = col ? FP8Q_SILU(true, true) : FP8Q_SILU(true, false);
+    else
+        e = col ? FP8Q_SILU(false, true) : FP8Q_SILU(false, false);
+#undef FP8Q_SILU
+    return launch_status(e);
 }
 
 int fp8q_rms_norm_per_block_quant(const void *x, void *residual, const void *weight, void *q,
@@ -177,36 +202,31 @@ int fp8q_rms_norm_per_block_quant(const void *x, void *residual, const void *wei
     if (!aligned(weight, 16) || (residual && !aligned(residual, 16)))
         return FP8Q_ERR_MISALIGNED;
     if (T > 0x7FFFFFFF)
-        return FP8Q_ERR_INVALID_ARG;
+        return FP8Q_ERR_UNSUPPORTED;
     const int G = int(H / kGroup);
-    int P = 8;
-    for (int p : {2, 4, 8}) {
-        if ((G + 2 * p - 1) / (2 * p) <= 32) {
-            P = p;
-            break;
-        }
-    }
-    if (G <= 2)
-        P = 1;
+    const bool longrow = G > 64;   // rows above 8192 values: one row per CTA, up to 1024 threads
     auto st = static_cast<cudaStream_t>(stream);
     auto xp = static_cast<const uint16_t *>(x);
     auto rp = static_cast<uint16_t *>(residual);
     auto wp = static_cast<const uint16_t *>(weight);
     auto qp = static_cast<uint8_t *>(q);
     const bool col = scale_layout == FP8Q_SCALES_COL_MAJOR;
+    const bool v8 = aligned(x, 32) && aligned(q, 32) && aligned(weight, 32) && (!rp || aligned(rp, 32));
     const int h = int(H);
-#define FP8Q_RMS(U, C)                                                                           \
-    (rp ? launch_rms<U, C, true>(P, xp, rp, wp, qp, scales, T, h, G, eps, st)                    \
-        : launch_rms<U, C, false>(P, xp, rp, wp, qp, scales, T, h, G, eps, st))
-    if (ue8m0) {
-        if (col) FP8Q_RMS(true, true);
-        else     FP8Q_RMS(true, false);
-    } else {
-        if (col) FP8Q_RMS(false, true);
-        else     FP8Q_RMS(false, false);
-    }
+    cudaError_t e;
+#define FP8Q_RMS_L(U, C, R, V)                                                                   \
+    (longrow ? launch_rms<U, C, R, V, true>(xp, rp, wp, qp, scales, T, h, G, eps, st)           \
+             : launch_rms<U, C, R, V, false>(xp, rp, wp, qp, scales, T, h, G, eps, st))
+#define FP8Q_RMS_V(U, C, R) (v8 ? FP8Q_RMS_L(U, C, R, true) : FP8Q_RMS_L(U, C, R, false))
+#define FP8Q_RMS(U, C) (rp ? FP8Q_RMS_V(U, C, true) : FP8Q_RMS_V(U, C, false))
+    if (ue8m0)
+        e = col ? FP8Q_RMS(true, true) : FP8Q_RMS(true, false);
+    else
+        e = col ? FP8Q_RMS(false, true) : FP8Q_RMS(false, false);
 #undef FP8Q_RMS
-    return launch_status();
+#undef FP8Q_RMS_V
+#undef FP8Q_RMS_L
+    return launch_status(e);
 }
 
 int fp8q_f32_to_e4m3(const float *v, void *out, int64_t n, void *stream)
@@ -219,13 +239,12 @@ int fp8q_f32_to_e4m3(const float *v, void *out, int64_t n, void *stream)
         return FP8Q_ERR_INVALID_ARG;
     if (!aligned(v, 16) || !aligned(out, 16))
         return FP8Q_ERR_MISALIGNED;
-    const int64_t threads = (n + 3) / 4;
-    const dim3 grid(unsigned((threads + 255) / 256));
-    if (grid.x == 0 || (threads + 255) / 256 > 0x7FFFFFFF)
-        return FP8Q_ERR_INVALID_ARG;
-    f32_to_e4m3_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+    const int64_t blocks = ((n + 3) / 4 + 255) / 256;
+    if (blocks > 0x7FFFFFFF)
+        return FP8Q_ERR_UNSUPPORTED;
+    f32_to_e4m3_kernel<<<dim3{unsigned(blocks)}, 256, 0, static_cast<cudaStream_t>(stream)>>>(
         v, static_cast<uint8_t *>(out), n);
-    return launch_status();
+    return launch_status(cudaSuccess);
 }
 
 const char *fp8q_status_string(int status)
@@ -233,13 +252,13 @@ const char *fp8q_status_string(int status)
     switch (status) {
     case FP8Q_OK: return "FP8Q_OK";
     case FP8Q_ERR_INVALID_ARG: return "FP8Q_ERR_INVALID_ARG: invalid argument";
-    case FP8Q_ERR_UNSUPPORTED: return "FP8Q_ERR_UNSUPPORTED: unsupported group size or row length";
+    case FP8Q_ERR_UNSUPPORTED: return "FP8Q_ERR_UNSUPPORTED: unsupported group size or size";
     case FP8Q_ERR_MISALIGNED: return "FP8Q_ERR_MISALIGNED: pointer not aligned as required";
     case FP8Q_ERR_CUDA: return "FP8Q_ERR_CUDA: CUDA launch failed";
     default: return "unknown fp8q status";
     }
 }
 
-int fp8q_version(void) { return 100; }
+int fp8q_version(void) { return 200; }
 
 }  // extern "C"

@@ -1,11 +1,14 @@
 // Device helpers shared by the three quantisation kernels: vector memory
-// access, bf16 unpacking, the half-warp group reduction, the group scale,
-// the correctly rounded quotient and the packed e4m3 conversion.
+// access, dependent-launch control, bf16 unpacking, the group reduction, the
+// group scale, the correctly rounded quotient and the packed e4m3 conversion.
 //
-// A group is 128 consecutive bf16 values of one token row (the Block_FP8
-// "1x128 activation scaling" of "Helion：用自动调优改进 vLLM 推理", section
-// Scope).  It is held by one half-warp: 16 lanes x 8 values, one 16-byte load
-// per lane, so a warp covers two groups = 512 contiguous bytes per load.
+// A group is 128 consecutive values of one token row (the Block_FP8 "1x128
+// activation scaling" of "Helion：用自动调优改进 vLLM 推理", section Scope).
+// It is held by a quad of 4 consecutive lanes, 32 values per lane (64 bytes of
+// bf16: two 256-bit loads on sm_100+ parts, four 128-bit loads when the
+// buffers are only 16-byte aligned), so a warp covers 8 groups.  The per-group
+// work (two shuffles, the scale, its reciprocal) is then spread over 32
+// values per lane.
 #pragma once
 
 #include <cstdint>
@@ -14,49 +17,149 @@
 namespace fp8q {
 
 constexpr int kGroup = 128;
-constexpr int kLanesPerGroup = 16;  // half-warp
-constexpr int kValsPerLane = 8;     // one 16-byte bf16 vector
+constexpr int kLanesPerGroup = 4;   // a quad
+constexpr int kValsPerLane = 32;    // 64 bytes of bf16, 32 bytes of e4m3
 constexpr float kFp8Max = 448.0f;   // largest finite float8_e4m3fn
 constexpr float kScaleFloor = 1e-10f;
 
 // ------------------------------------------------------------- memory ---
+//
+// All loads are volatile inline PTX with a "memory" clobber, issued only on
+// addresses the caller has clamped into its buffer, so no access can leave
+// the buffer whatever the compiler schedules.  V8 selects 256-bit accesses
+// (32-byte aligned buffers) over 128-bit ones.
 
-// Loads and stores go through CUDA's intrinsics rather than inline asm so the
-// compiler treats them as memory accesses that may fault and never hoists one
-// above the bounds check that guards it.
+#define FP8Q_LD4(QUAL, p, a, b, c, d)                                                        \
+    asm volatile("ld.global" QUAL ".v4.b32 {%0,%1,%2,%3}, [%4];"                              \
+                 : "=r"(a), "=r"(b), "=r"(c), "=r"(d)                                         \
+                 : "l"(p)                                                                     \
+                 : "memory")
+#define FP8Q_LD8(QUAL, p, w, o)                                                              \
+    asm volatile("ld.global" QUAL ".v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"                  \
+                 : "=r"(w[o + 0]), "=r"(w[o + 1]), "=r"(w[o + 2]), "=r"(w[o + 3]),             \
+                   "=r"(w[o + 4]), "=r"(w[o + 5]), "=r"(w[o + 6]), "=r"(w[o + 7])              \
+                 : "l"(p)                                                                     \
+                 : "memory")
 
-// 16-byte load of data read exactly once (ld.global.cs: evict-first).
-__device__ __forceinline__ uint4 ld_stream16(const void *p)
+// 64 bytes read once (streamed input): read-only path, L2 evict-first.
+template <bool V8>
+__device__ __forceinline__ void ld64_stream(const void *p, uint32_t (&w)[16])
 {
-    return __ldcs(reinterpret_cast<const uint4 *>(p));
+    const char *c = static_cast<const char *>(p);
+    if (V8) {
+        FP8Q_LD8(".nc.L1::no_allocate.L2::evict_first", c, w, 0);
+        FP8Q_LD8(".nc.L1::no_allocate.L2::evict_first", c + 32, w, 8);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            FP8Q_LD4(".nc.L1::no_allocate", c + 16 * k, w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+    }
 }
 
-// 16-byte load of data every CTA re-reads (the RMSNorm weight): read-only path.
-__device__ __forceinline__ uint4 ld_keep16(const void *p)
+// 64 bytes every CTA re-reads (the RMSNorm weight): read-only, kept in L2.
+template <bool V8>
+__device__ __forceinline__ void ld64_keep(const void *p, uint32_t (&w)[16])
 {
-    return __ldg(reinterpret_cast<const uint4 *>(p));
+    const char *c = static_cast<const char *>(p);
+    if (V8) {
+        FP8Q_LD8(".nc.L2::evict_last", c, w, 0);
+        FP8Q_LD8(".nc.L2::evict_last", c + 32, w, 8);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            FP8Q_LD4(".nc", c + 16 * k, w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+    }
 }
 
-// 16-byte load of data this kernel also writes (the residual).
-__device__ __forceinline__ uint4 ld_rw16(const void *p)
+// 64 bytes this kernel also writes (the residual): coherent path.
+template <bool V8>
+__device__ __forceinline__ void ld64_rw(const void *p, uint32_t (&w)[16])
 {
-    return *reinterpret_cast<const uint4 *>(p);
+    const char *c = static_cast<const char *>(p);
+    if (V8) {
+        FP8Q_LD8(".L1::no_allocate.L2::evict_first", c, w, 0);
+        FP8Q_LD8(".L1::no_allocate.L2::evict_first", c + 32, w, 8);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            FP8Q_LD4(".L1::no_allocate", c + 16 * k, w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+    }
 }
 
-__device__ __forceinline__ void st16(void *p, uint4 v) { *reinterpret_cast<uint4 *>(p) = v; }
+template <bool V8>
+__device__ __forceinline__ void st64(void *p, const uint32_t (&w)[16])
+{
+    char *c = static_cast<char *>(p);
+    if (V8) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(c + 32 * h),
+                         "r"(w[8 * h]), "r"(w[8 * h + 1]), "r"(w[8 * h + 2]), "r"(w[8 * h + 3]),
+                         "r"(w[8 * h + 4]), "r"(w[8 * h + 5]), "r"(w[8 * h + 6]), "r"(w[8 * h + 7])
+                         : "memory");
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(c + 16 * k), "r"(w[4 * k]),
+                         "r"(w[4 * k + 1]), "r"(w[4 * k + 2]), "r"(w[4 * k + 3])
+                         : "memory");
+    }
+}
 
-__device__ __forceinline__ void st8(void *p, uint2 v) { *reinterpret_cast<uint2 *>(p) = v; }
+// 32 e4m3 codes (32 bytes).
+template <bool V8>
+__device__ __forceinline__ void st32(void *p, const uint32_t (&w)[8])
+{
+    char *c = static_cast<char *>(p);
+    if (V8) {
+        asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(c), "r"(w[0]),
+                     "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                     : "memory");
+    } else {
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+            asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(c + 16 * k), "r"(w[4 * k]),
+                         "r"(w[4 * k + 1]), "r"(w[4 * k + 2]), "r"(w[4 * k + 3])
+                         : "memory");
+    }
+}
+
+// ------------------------------------------------ dependent launches ---
+//
+// Every kernel is launched with programmatic stream serialization allowed,
+// so on a stream (or in a CUDA graph) it may start while the kernel before it
+// drains.  It therefore waits for that kernel's completion and memory flush
+// (griddepcontrol.wait) before its first global load or store, and lets the
+// kernel after it begin launching once all of its own CTAs are running.
+// Without the launch attribute both instructions are no-ops.
+
+__device__ __forceinline__ void wait_for_producer()
+{
+#ifndef FP8Q_NO_PDL
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+}
+
+__device__ __forceinline__ void allow_consumer_launch()
+{
+#ifndef FP8Q_NO_PDL
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+}
 
 // --------------------------------------------------------------- bf16 ---
 
 // bf16 -> fp32 is exact: the bf16 bits are the top half of the fp32 bits.
-__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8])
+// Word k holds values 2k (low half, lower address) and 2k+1.
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ void unpack32(const uint32_t (&w)[16], float (&f)[32])
 {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        f[2 * k] = __uint_as_float(w[k] << 16);          // lower address
-        f[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    for (int k = 0; k < 16; ++k) {
+        f[2 * k] = bf_lo(w[k]);
+        f[2 * k + 1] = bf_hi(w[k]);
     }
 }
 
@@ -70,13 +173,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 
 // ------------------------------------------------------- reductions ---
 
-// Max over the 16 lanes of a half-warp.  Every lane of the warp must call it
-// (the shuffles name the full mask); the two half-warps reduce independently.
-__device__ __forceinline__ float halfwarp_max(float m)
+// Max over the 4 lanes of a quad.  Every lane of the warp calls it (the
+// shuffles name the full mask); the 8 quads reduce independently.
+__device__ __forceinline__ float quad_max(float m)
 {
-#pragma unroll
-    for (int o = 8; o >= 1; o >>= 1)
-        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
     return m;
 }
 
@@ -86,6 +188,17 @@ __device__ __forceinline__ float warp_sum(float s)
     for (int o = 16; o >= 1; o >>= 1)
         s = __fadd_rn(s, __shfl_xor_sync(0xFFFFFFFFu, s, o));
     return s;
+}
+
+__device__ __forceinline__ float absmax32(const float (&v)[32])
+{
+    float m0 = fabsf(v[0]), m1 = fabsf(v[1]);
+#pragma unroll
+    for (int k = 2; k < 32; k += 2) {
+        m0 = fmaxf(m0, fabsf(v[k]));
+        m1 = fmaxf(m1, fabsf(v[k + 1]));
+    }
+    return fmaxf(m0, m1);
 }
 
 // ------------------------------------------------------------ scale -----
@@ -106,35 +219,41 @@ __device__ __forceinline__ float group_scale(float amax, float eps)
     return s;
 }
 
-// Correctly rounded |x| / s, given r = RN32(1/s).
-//
-// Power-of-two s: r is exactly 1/s, so one multiply is the exact quotient
-// rounded once.  Otherwise: y0 = RN(x r) is within 1.5 ulp of x/s; one
-// residual step y1 = RN(y0 + RN(x - s y0) r) makes it faithful; a second
-// step with the exact residual x - s y1 (an FMA) then yields RN32(x/s) by
-// Markstein's theorem (P. Markstein, "Computation of elementary functions on
-// the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990: a
-// faithful quotient corrected with a correctly rounded reciprocal and an
-// exact FMA residual is the correctly rounded quotient, barring underflow).
-// Underflow only happens for quotients far below 2^-10, whose e4m3 code is
-// zero either way.  Working on |x| keeps the sign of zero out of the
-// arithmetic; the caller restores it.
-template <bool POW2>
-__device__ __forceinline__ float quotient_abs(float ax, float s, float r)
+// 1/s: exact for a power of two (2^k has biased exponent k+127, 2^-k has
+// 127-k = 254 - that; s lies in [2^-108, 2^120] for finite inputs, so both
+// are normal), otherwise the correctly rounded reciprocal.
+template <bool UE8M0>
+__device__ __forceinline__ float scale_recip(float s)
 {
-    float y = __fmul_rn(ax, r);
-    if (POW2)
-        return y;
-    float e = __fmaf_rn(-y, s, ax);
-    y = __fmaf_rn(e, r, y);
-    e = __fmaf_rn(-y, s, ax);
-    return __fmaf_rn(e, r, y);
+    if (UE8M0)
+        return __uint_as_float(0x7F000000u - (__float_as_uint(s) & 0x7F800000u));
+    return __frcp_rn(s);
 }
 
+// Correctly rounded x / s, given r = RN32(1/s).
+//
+// Power-of-two s: r is exactly 1/s, so one multiply is the exact quotient
+// rounded once (its sign, zero included, is the sign of x).  Otherwise, on
+// |x|: y0 = RN(|x| r) is within 1.5 ulp of |x|/s; one residual step
+// y1 = RN(y0 + RN(|x| - s y0) r) makes it faithful; a second step with the
+// exact residual |x| - s y1 (an FMA) then yields RN32(|x|/s) by Markstein's
+// theorem (P. Markstein, "Computation of elementary functions on the IBM
+// RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990: a faithful
+// quotient corrected with a correctly rounded reciprocal and an exact FMA
+// residual is the correctly rounded quotient, barring underflow).  Underflow
+// only happens for quotients far below 2^-10, whose e4m3 code is zero either
+// way.  The sign of x, zero included, is put back last.
 template <bool POW2>
 __device__ __forceinline__ float quotient(float x, float s, float r)
 {
-    return copysignf(quotient_abs<POW2>(fabsf(x), s, r), x);
+    if (POW2)
+        return __fmul_rn(x, r);
+    const float ax = fabsf(x);
+    float y = __fmul_rn(ax, r);
+    float e = __fmaf_rn(-y, s, ax);
+    y = __fmaf_rn(e, r, y);
+    e = __fmaf_rn(-y, s, ax);
+    return copysignf(__fmaf_rn(e, r, y), x);
 }
 
 // --------------------------------------------------------------- e4m3 ---
@@ -154,27 +273,14 @@ __device__ __forceinline__ uint32_t pack4_e4m3(float a0, float a1, float a2, flo
     return r;
 }
 
-// Quantise the 8 values a lane holds with its group's scale; returns 8 codes.
+// Quantise the 32 values of a lane with its group's scale into 32 codes.
 template <bool UE8M0>
-__device__ __forceinline__ uint2 quant8(const float (&v)[8], float s, float r)
+__device__ __forceinline__ void quant32(const float (&v)[32], float s, float r, uint32_t (&c)[8])
 {
-    float p[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k)
-        p[k] = quotient<UE8M0>(v[k], s, r);
-    uint2 out;
-    out.x = pack4_e4m3(p[0], p[1], p[2], p[3]);
-    out.y = pack4_e4m3(p[4], p[5], p[6], p[7]);
-    return out;
-}
-
-__device__ __forceinline__ float absmax8(const float (&v)[8])
-{
-    float m = fabsf(v[0]);
-#pragma unroll
-    for (int k = 1; k < 8; ++k)
-        m = fmaxf(m, fabsf(v[k]));
-    return m;
+        c[k] = pack4_e4m3(quotient<UE8M0>(v[4 * k], s, r), quotient<UE8M0>(v[4 * k + 1], s, r),
+                          quotient<UE8M0>(v[4 * k + 2], s, r), quotient<UE8M0>(v[4 * k + 3], s, r));
 }
 
 }  // namespace fp8q

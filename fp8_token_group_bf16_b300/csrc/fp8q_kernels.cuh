@@ -1,64 +1,75 @@
 // The three quantisation kernels for sm_103a.
 //
 // All three are HBM-bound streaming kernels: a handful of fp32 operations per
-// byte moved, no contraction, so no tensor cores.  Each lane moves its data
-// with 16-byte vector loads issued before any arithmetic, so a thread keeps
-// several independent loads in flight.
+// byte moved, no contraction, so no tensor cores.  A quad of lanes owns a
+// group (32 values per lane); every lane issues all of its loads before any
+// arithmetic so several 64-byte requests per thread are in flight.
 #pragma once
 
 #include "fp8q_device.cuh"
 
 namespace fp8q {
 
-// Index of a group's scale in the chosen layout (row t, group g of G).
-template <bool COL>
-__device__ __forceinline__ int64_t scale_index(int64_t t, int64_t g, int64_t T, int64_t G)
+constexpr int kCtaThreads = 256;                               // ops A and C
+constexpr int kGroupsPerCta = kCtaThreads / kLanesPerGroup;    // 64
+constexpr int kGroupQuantGpt = 2;                              // groups per quad, op A
+
+// Row t and group g of flat group index gi (G groups per row).  The host
+// guarantees T*G < 2^31 (2^38 bf16 values would not fit in HBM anyway), so a
+// 32-bit division suffices.
+__device__ __forceinline__ void split_group(int64_t gi, int64_t G, int64_t &t, int64_t &g)
 {
-    return COL ? g * T + t : t * G + g;
+    const uint32_t tt = uint32_t(gi) / uint32_t(G);
+    t = tt;
+    g = gi - int64_t(tt) * G;
 }
 
 // --------------------------------------------------------------------------
 // per_token_group_fp8_quant
 //
 // A contiguous [T, H] tensor is a flat sequence of T*G groups, so the kernel
-// walks groups, not rows: half-warp h of CTA b handles groups
-// b*HPB*GPT + j*HPB + h for j < GPT (HPB half-warps per CTA).  The two
-// half-warps of a warp take adjacent groups, so every load instruction of a
-// warp reads 512 contiguous bytes.  All GPT loads are issued first.
+// walks groups, not rows.  CTA b owns groups [b*64*GPT, (b+1)*64*GPT); quad q
+// of the CTA takes groups b*64*GPT + j*64 + q for j < GPT, so the 8 quads of
+// a warp read 8 adjacent groups (2 KiB) per pair of load instructions.
+// Out-of-range quads load a clamped, valid group and store nothing.
 // --------------------------------------------------------------------------
-template <bool UE8M0, bool COL, int GPT>
-__global__ void __launch_bounds__(256) group_quant_kernel(const uint16_t *__restrict__ x,
-                                                          uint8_t *__restrict__ q,
-                                                          float *__restrict__ scales,
-                                                          int64_t n_groups, int64_t G, int64_t T,
-                                                          float eps)
+template <bool UE8M0, bool COL, bool V8>
+__global__ void __launch_bounds__(kCtaThreads) group_quant_kernel(const uint16_t *__restrict__ x,
+                                                                  uint8_t *__restrict__ q,
+                                                                  float *__restrict__ scales,
+                                                                  int64_t n_groups, int64_t G,
+                                                                  int64_t T, float eps)
 {
-    const int lane = threadIdx.x & (kLanesPerGroup - 1);
-    const int hpb = blockDim.x / kLanesPerGroup;
-    const int64_t first = int64_t(blockIdx.x) * hpb * GPT + (threadIdx.x / kLanesPerGroup);
+    constexpr int GPT = kGroupQuantGpt;
+    const int sub = threadIdx.x & (kLanesPerGroup - 1);
+    const int64_t first = int64_t(blockIdx.x) * kGroupsPerCta * GPT + (threadIdx.x / kLanesPerGroup);
 
-    uint4 raw[GPT];
+    wait_for_producer();
+    allow_consumer_launch();
+    uint32_t raw[GPT][16];
 #pragma unroll
     for (int j = 0; j < GPT; ++j) {
-        const int64_t gi = first + int64_t(j) * hpb;
-        raw[j] = gi < n_groups ? ld_stream16(x + gi * kGroup + lane * kValsPerLane)
-                               : make_uint4(0u, 0u, 0u, 0u);
+        const int64_t gi = first + int64_t(j) * kGroupsPerCta;
+        const int64_t gl = gi < n_groups ? gi : n_groups - 1;
+        ld64_stream<V8>(x + gl * kGroup + sub * kValsPerLane, raw[j]);
     }
 #pragma unroll
     for (int j = 0; j < GPT; ++j) {
-        const int64_t gi = first + int64_t(j) * hpb;
-        float v[8];
-        unpack8(raw[j], v);
-        const float amax = halfwarp_max(absmax8(v));
+        const int64_t gi = first + int64_t(j) * kGroupsPerCta;
+        float v[32];
+        unpack32(raw[j], v);
+        const float amax = quad_max(absmax32(v));
         const float s = group_scale<UE8M0>(amax, eps);
-        const float r = __frcp_rn(s);
-        const uint2 codes = quant8<UE8M0>(v, s, r);
+        const float r = scale_recip<UE8M0>(s);
+        uint32_t codes[8];
+        quant32<UE8M0>(v, s, r, codes);
         if (gi < n_groups) {
-            st8(q + gi * kGroup + lane * kValsPerLane, codes);
-            if (lane == 0) {
+            st32<V8>(q + gi * kGroup + sub * kValsPerLane, codes);
+            if (sub == 0) {
                 if (COL) {
-                    const int64_t t = gi / G;
-                    scales[scale_index<true>(t, gi - t * G, T, G)] = s;
+                    int64_t t, g;
+                    split_group(gi, G, t, g);
+                    scales[g * T + t] = s;
                 } else {
                     scales[gi] = s;
                 }
@@ -70,8 +81,9 @@ __global__ void __launch_bounds__(256) group_quant_kernel(const uint16_t *__rest
 // --------------------------------------------------------------------------
 // silu_and_mul_per_block_quant
 //
-// Same group walk over the T*G output groups; output group (t, g) reads the
-// gate vector at x[t, g*128 ...] and the up vector at x[t, I + g*128 ...].
+// One output group per quad: output group gi = (t, g) reads the gate values
+// x[t, g*128 ...] and the up values x[t, I + g*128 ...] (64 bytes of each per
+// lane, both loads issued first).
 // --------------------------------------------------------------------------
 __device__ __forceinline__ float silu_mul(float a, float b)
 {
@@ -79,155 +91,151 @@ __device__ __forceinline__ float silu_mul(float a, float b)
     return __fmul_rn(__fdiv_rn(a, d), b);
 }
 
-template <bool UE8M0, bool COL, int GPT>
-__global__ void __launch_bounds__(256) silu_quant_kernel(const uint16_t *__restrict__ x,
-                                                         uint8_t *__restrict__ q,
-                                                         float *__restrict__ scales,
-                                                         int64_t n_groups, int64_t G, int64_t T,
-                                                         int64_t I, float eps)
+template <bool UE8M0, bool COL, bool V8>
+__global__ void __launch_bounds__(kCtaThreads) silu_quant_kernel(const uint16_t *__restrict__ x,
+                                                                 uint8_t *__restrict__ q,
+                                                                 float *__restrict__ scales,
+                                                                 int64_t n_groups, int64_t G,
+                                                                 int64_t T, int64_t I, float eps)
 {
-    const int lane = threadIdx.x & (kLanesPerGroup - 1);
-    const int hpb = blockDim.x / kLanesPerGroup;
-    const int64_t first = int64_t(blockIdx.x) * hpb * GPT + (threadIdx.x / kLanesPerGroup);
+    const int sub = threadIdx.x & (kLanesPerGroup - 1);
+    const int64_t gi = int64_t(blockIdx.x) * kGroupsPerCta + (threadIdx.x / kLanesPerGroup);
+    const int64_t gl = gi < n_groups ? gi : n_groups - 1;
+    int64_t t, g;
+    split_group(gl, G, t, g);
+    const uint16_t *pa = x + t * 2 * I + g * kGroup + sub * kValsPerLane;
+    wait_for_producer();
+    allow_consumer_launch();
+    uint32_t ra[16], rb[16];
+    ld64_stream<V8>(pa, ra);
+    ld64_stream<V8>(pa + I, rb);
 
-    uint4 ra[GPT], rb[GPT];
-    int64_t row[GPT];
+    float v[32];
 #pragma unroll
-    for (int j = 0; j < GPT; ++j) {
-        const int64_t gi = first + int64_t(j) * hpb;
-        const int64_t t = gi / G;
-        row[j] = t;
-        const int64_t off = t * 2 * I + (gi - t * G) * kGroup + lane * kValsPerLane;
-        const bool ok = gi < n_groups;
-        ra[j] = ok ? ld_stream16(x + off) : make_uint4(0u, 0u, 0u, 0u);
-        rb[j] = ok ? ld_stream16(x + off + I) : make_uint4(0u, 0u, 0u, 0u);
+    for (int k = 0; k < 16; ++k) {
+        v[2 * k] = silu_mul(bf_lo(ra[k]), bf_lo(rb[k]));
+        v[2 * k + 1] = silu_mul(bf_hi(ra[k]), bf_hi(rb[k]));
     }
-#pragma unroll
-    for (int j = 0; j < GPT; ++j) {
-        const int64_t gi = first + int64_t(j) * hpb;
-        float a[8], b[8], v[8];
-        unpack8(ra[j], a);
-        unpack8(rb[j], b);
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            v[k] = silu_mul(a[k], b[k]);
-        const float amax = halfwarp_max(absmax8(v));
-        const float s = group_scale<UE8M0>(amax, eps);
-        const float r = __frcp_rn(s);
-        const uint2 codes = quant8<UE8M0>(v, s, r);
-        if (gi < n_groups) {
-            st8(q + gi * kGroup + lane * kValsPerLane, codes);
-            if (lane == 0)
-                scales[COL ? scale_index<true>(row[j], gi - row[j] * G, T, G) : gi] = s;
-        }
+    const float amax = quad_max(absmax32(v));
+    const float s = group_scale<UE8M0>(amax, eps);
+    const float r = scale_recip<UE8M0>(s);
+    uint32_t codes[8];
+    quant32<UE8M0>(v, s, r, codes);
+    if (gi < n_groups) {
+        st32<V8>(q + gi * kGroup + sub * kValsPerLane, codes);
+        if (sub == 0)
+            scales[COL ? g * T + t : gi] = s;
     }
 }
 
 // --------------------------------------------------------------------------
-// rms_norm_per_block_quant, one CTA per token row.
+// rms_norm_per_block_quant
 //
-// blockDim = 32 * W threads, W = ceil(G / (2P)); half-warp h holds groups
-// h, h + 2W, ..., (P of them), all loaded before any arithmetic.  The row's
-// sum of squares is reduced per thread (sequential fma over its values), per
-// warp (butterfly), then across warps through shared memory in warp order,
-// so every thread ends with the same value.  The optional residual add
-// z = bf16(x + r) is written back before the norm.
+// A CTA of 4*G lanes (rounded up to whole warps) owns whole rows: quad g
+// holds group g of the row, 32 values per lane.  The row's sum of squares is
+// reduced per lane (two interleaved fma chains), per warp (butterfly) and
+// across warps through shared memory in warp order, so every lane gets the
+// same value.  Lanes past the end of the row (G not a multiple of 8) hold a
+// clamped copy of group G-1 and add nothing.
+//
+// Rows of up to 8192 values (<= 256 threads, !LONG): the CTA is persistent
+// (grid = resident CTAs, rows t = blockIdx.x + k*gridDim.x), keeps its slice
+// of the weight in registers across rows, and loads row t + gridDim.x while
+// it reduces and quantises row t.  Longer rows (LONG, <= 1024 threads) take
+// one row per CTA and read the weight after the reduction.
 // --------------------------------------------------------------------------
-template <bool UE8M0, bool COL, bool RES, int P>
-__global__ void __launch_bounds__(1024) rms_quant_kernel(const uint16_t *__restrict__ x,
-                                                         uint16_t *__restrict__ residual,
-                                                         const uint16_t *__restrict__ w,
-                                                         uint8_t *__restrict__ q,
-                                                         float *__restrict__ scales, int64_t T,
-                                                         int H, int G, float eps)
+template <bool RES, bool V8>
+__device__ __forceinline__ void load_row(const uint16_t *x, const uint16_t *residual, int64_t off,
+                                         uint32_t (&xr)[16], uint32_t (&rr)[16])
 {
-    __shared__ float part[32];
-    const int64_t t = blockIdx.x;
-    const int lane = threadIdx.x & (kLanesPerGroup - 1);
-    const int hw = threadIdx.x / kLanesPerGroup;
-    const int hpb = blockDim.x / kLanesPerGroup;
-    const int nwarps = blockDim.x / 32;
+    ld64_stream<V8>(x + off, xr);
+    if (RES)
+        ld64_rw<V8>(residual + off, rr);
+}
 
-    // Short rows load the weight with the row; long rows (P > 2) re-read it
-    // from L1/L2 at the end instead of holding it in registers.
-    constexpr bool kWeightEarly = P <= 2;
-    constexpr int PW = kWeightEarly ? P : 1;
-    uint4 rz[P], rw[PW];
+template <bool UE8M0, bool COL, bool RES, bool V8, bool LONG>
+__global__ void __launch_bounds__(LONG ? 1024 : 256) rms_quant_kernel(
+    const uint16_t *__restrict__ x, uint16_t *__restrict__ residual, const uint16_t *__restrict__ w,
+    uint8_t *__restrict__ q, float *__restrict__ scales, int64_t T, int H, int G, float eps)
+{
+    __shared__ float part[2][32];
+    const int sub = threadIdx.x & (kLanesPerGroup - 1);
+    const int g = threadIdx.x / kLanesPerGroup;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const bool ok = g < G;
+    const int col = (ok ? g : G - 1) * kGroup + sub * kValsPerLane;   // clamped into the row
+
+    wait_for_producer();
+    allow_consumer_launch();
+    uint32_t wr[16];
+    if (!LONG)
+        ld64_keep<V8>(w + col, wr);
+
+    int64_t t = blockIdx.x;
+    uint32_t cx[16], cr[16];
+    load_row<RES, V8>(x, residual, t * H + col, cx, cr);
+
+    for (int it = 0; t < T; ++it, t += gridDim.x) {
+        uint32_t nx[16], nr[16];
+        const int64_t tn = t + gridDim.x;
+        if (!LONG && tn < T) {
+            load_row<RES, V8>(x, residual, tn * H + col, nx, nr);
+        } else {
 #pragma unroll
-    for (int j = 0; j < P; ++j) {
-        const int g = hw + j * hpb;
-        const int64_t off = t * H + int64_t(g) * kGroup + lane * kValsPerLane;
-        const bool ok = g < G;
-        rz[j] = ok ? ld_stream16(x + off) : make_uint4(0u, 0u, 0u, 0u);
-        if (kWeightEarly)
-            rw[j % PW] = ok ? ld_keep16(w + g * kGroup + lane * kValsPerLane) : make_uint4(0u, 0u, 0u, 0u);
-    }
-    if (RES) {
-        uint4 rr[P];
-#pragma unroll
-        for (int j = 0; j < P; ++j) {
-            const int g = hw + j * hpb;
-            const int64_t off = t * H + int64_t(g) * kGroup + lane * kValsPerLane;
-            rr[j] = g < G ? ld_rw16(residual + off) : make_uint4(0u, 0u, 0u, 0u);
+            for (int k = 0; k < 16; ++k)
+                nx[k] = nr[k] = 0u;
         }
+
+        if (RES) {
+            // z = bf16(x + r), written back to the residual, is what is normalised
 #pragma unroll
-        for (int j = 0; j < P; ++j) {
-            const int g = hw + j * hpb;
-            float a[8], b[8];
-            unpack8(rz[j], a);
-            unpack8(rr[j], b);
-            uint4 z;
-            z.x = pack_bf16x2(__fadd_rn(a[0], b[0]), __fadd_rn(a[1], b[1]));
-            z.y = pack_bf16x2(__fadd_rn(a[2], b[2]), __fadd_rn(a[3], b[3]));
-            z.z = pack_bf16x2(__fadd_rn(a[4], b[4]), __fadd_rn(a[5], b[5]));
-            z.w = pack_bf16x2(__fadd_rn(a[6], b[6]), __fadd_rn(a[7], b[7]));
-            rz[j] = z;
-            if (g < G)
-                st16(residual + t * H + int64_t(g) * kGroup + lane * kValsPerLane, z);
+            for (int k = 0; k < 16; ++k)
+                cx[k] = pack_bf16x2(__fadd_rn(bf_lo(cx[k]), bf_lo(cr[k])), __fadd_rn(bf_hi(cx[k]), bf_hi(cr[k])));
+            if (ok)
+                st64<V8>(residual + t * H + col, cx);
         }
-    }
 
-    float ss = 0.0f;
+        float ss0 = 0.0f, ss1 = 0.0f;
 #pragma unroll
-    for (int j = 0; j < P; ++j) {
-        float z[8];
-        unpack8(rz[j], z);
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            ss = __fmaf_rn(z[k], z[k], ss);
-    }
-    ss = warp_sum(ss);
-    if ((threadIdx.x & 31) == 0)
-        part[threadIdx.x >> 5] = ss;
-    __syncthreads();
-    float tot = 0.0f;
-    for (int i = 0; i < nwarps; ++i)
-        tot = __fadd_rn(tot, part[i]);
+        for (int k = 0; k < 16; ++k) {
+            ss0 = __fmaf_rn(bf_lo(cx[k]), bf_lo(cx[k]), ss0);
+            ss1 = __fmaf_rn(bf_hi(cx[k]), bf_hi(cx[k]), ss1);
+        }
+        const float ssw = warp_sum(ok ? __fadd_rn(ss0, ss1) : 0.0f);
+        if ((threadIdx.x & 31) == 0)
+            part[it & 1][warp] = ssw;
+        __syncthreads();
+        float tot = 0.0f;
+        for (int i = 0; i < nwarps; ++i)
+            tot = __fadd_rn(tot, part[it & 1][i]);
 
-    const float mean = __fdiv_rn(tot, float(H));
-    const float rstd = __fsqrt_rn(__fadd_rn(mean, eps));
-    const float inv = __frcp_rn(rstd);
+        const float mean = __fdiv_rn(tot, float(H));
+        const float rstd = __fsqrt_rn(__fadd_rn(mean, eps));
+        const float inv = __frcp_rn(rstd);
 
+        if (LONG)
+            ld64_keep<V8>(w + col, wr);
+        float v[32];
 #pragma unroll
-    for (int j = 0; j < P; ++j) {
-        const int g = hw + j * hpb;
-        float z[8], wv[8], v[8];
-        unpack8(rz[j], z);
-        if (kWeightEarly)
-            unpack8(rw[j % PW], wv);
-        else
-            unpack8(g < G ? ld_keep16(w + g * kGroup + lane * kValsPerLane) : make_uint4(0u, 0u, 0u, 0u), wv);
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            v[k] = __fmul_rn(__fmul_rn(z[k], inv), wv[k]);
-        const float amax = halfwarp_max(absmax8(v));
+        for (int k = 0; k < 16; ++k) {
+            v[2 * k] = __fmul_rn(__fmul_rn(bf_lo(cx[k]), inv), bf_lo(wr[k]));
+            v[2 * k + 1] = __fmul_rn(__fmul_rn(bf_hi(cx[k]), inv), bf_hi(wr[k]));
+        }
+        const float amax = quad_max(absmax32(v));
         const float s = group_scale<UE8M0>(amax, kScaleFloor);
-        const float r = __frcp_rn(s);
-        const uint2 codes = quant8<UE8M0>(v, s, r);
-        if (g < G) {
-            st8(q + t * H + int64_t(g) * kGroup + lane * kValsPerLane, codes);
-            if (lane == 0)
-                scales[scale_index<COL>(t, g, T, G)] = s;
+        const float r = scale_recip<UE8M0>(s);
+        uint32_t codes[8];
+        quant32<UE8M0>(v, s, r, codes);
+        if (ok) {
+            st32<V8>(q + t * H + col, codes);
+            if (sub == 0)
+                scales[COL ? int64_t(g) * T + t : t * G + g] = s;
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            cx[k] = nx[k];
+            cr[k] = nr[k];
         }
     }
 }

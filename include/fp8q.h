@@ -57,7 +57,7 @@ extern "C" {
 typedef enum {
     FP8Q_OK = 0,
     FP8Q_ERR_INVALID_ARG = 1, /* negative T, H <= 0, H % group_size, NULL pointer, bad enum, bad eps */
-    FP8Q_ERR_UNSUPPORTED = 2, /* group_size != 128, or a row longer than the kernels handle */
+    FP8Q_ERR_UNSUPPORTED = 2, /* group_size != 128, a row longer than the kernels handle, T*G >= 2^31 */
     FP8Q_ERR_MISALIGNED = 3,  /* a pointer below its required alignment */
     FP8Q_ERR_CUDA = 4         /* the CUDA launch failed */
 } fp8q_status;
@@ -68,7 +68,7 @@ typedef enum {
 } fp8q_scale_layout;
 
 /* Longest rms_norm_per_block_quant row (H) the kernels accept. */
-#define FP8Q_RMS_MAX_H 65536
+#define FP8Q_RMS_MAX_H 32768
 
 /*
  * per_token_group_fp8_quant.
