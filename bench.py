@@ -477,25 +477,27 @@ def oracle_sample_run(host, rows: int) -> tuple[float, int]:
     return secs, step_bytes(rows)
 
 
-def cpu_baseline(host, target_s: float = 10.0) -> dict:
+def cpu_baseline(host, T: int = STEP_T, target_s: float = 10.0) -> dict:
     secs, _ = oracle_sample_run(host, 8)
-    rows = max(8, min(STEP_T, int(8 * target_s / max(secs, 1e-6))))
+    rows = max(8, min(T, int(8 * target_s / max(secs, 1e-6))))
     secs, nbytes = oracle_sample_run(host, rows)
     return {"value": round(nbytes / secs / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"first {rows} of {STEP_T} tokens of each of the three ops "
+            "sample": f"first {rows} of {T} tokens of each of the three ops "
                       f"({nbytes / 1e6:.1f} MB algorithmic, {secs:.1f} s, single-threaded C)"}
 
 
-def step_config() -> dict:
+def step_config(T: int = STEP_T) -> dict:
+    mb = step_bytes(T) / 1e6
     return {
-        "workload": f"Qwen3-32B-shaped FP8 quant epilogues, T={STEP_T} tokens per step: "
-                    f"per_token_group_fp8_quant [{STEP_T},{A_H}] heavy-tailed (UE8M0, column-major scales); "
-                    f"rms_norm_per_block_quant [{STEP_T},{B_H}] lognormal channels (UE8M0, row-major); "
-                    f"silu_and_mul_per_block_quant [{STEP_T},{2 * C_I}] lognormal channels (UE8M0, row-major); "
+        "workload": f"Qwen3-32B-shaped FP8 quant epilogues, T={T} tokens per step: "
+                    f"per_token_group_fp8_quant [{T},{A_H}] heavy-tailed (UE8M0, column-major scales); "
+                    f"rms_norm_per_block_quant [{T},{B_H}] lognormal channels (UE8M0, row-major); "
+                    f"silu_and_mul_per_block_quant [{T},{2 * C_I}] lognormal channels (UE8M0, row-major); "
                     "group 128",
-        "T": STEP_T, "H_group_quant": A_H, "H_rms": B_H, "I_silu": C_I, "group": GROUP,
-        "l2": "inputs larger than L2: a step touches 680 MB (> 5x the 126 MB L2), so every "
-              "buffer is evicted by the other two ops before it is read again",
+        "T": T, "H_group_quant": A_H, "H_rms": B_H, "I_silu": C_I, "group": GROUP,
+        "l2": (f"inputs larger than L2: a step touches {mb:.0f} MB (> 126 MB L2), so every "
+               "buffer is evicted by the other two ops before it is read again") if mb > 2 * 126
+              else f"a step touches {mb:.0f} MB, not much more than the 126 MB L2: not a bandwidth figure",
         "parallelism": "one independent batch per GPU (weak scaling, no collective)",
     }
 
@@ -629,6 +631,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--sweep", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--tokens", type=int, default=STEP_T,
+                   help="tokens per step (default: the T=4096 workload; smaller values are for profiling)")
     p.add_argument("--reference-budget-s", type=float, default=120.0,
                    help="CPU seconds the reference arm spends over all its steps")
     return p.parse_args(argv)
@@ -656,25 +660,26 @@ def main(argv=None):
         import fp8_token_group_bf16_b300 as fq
 
         fq.load()
-        host = workload_inputs(STEP_T)
+        T = args.tokens
+        host = workload_inputs(T)
         stream = torch.cuda.Stream()
-        step = DeviceStep(host, stream)
+        step = DeviceStep(host, stream, T)
         clocks = ClockSampler(torch.cuda.current_device()).start()
         try:
             secs, per_op_ms, window = time_device(step, args.steps, args.warmup, dist)
         finally:
             clocks.stop()
-        agg = aggregate(step_bytes() * args.steps, secs, dist, args.steps)
+        agg = aggregate(step_bytes(T) * args.steps, secs, dist, args.steps)
         peak, peak_kind = load_peaks()
         dom_ms = per_op_ms[DOMINANT]
         achieved = step.bytes[DOMINANT] / (dom_ms * 1e-3) / 1e9
-        traffic = recorded_traffic(KERNEL_NAMES[DOMINANT], f"T={STEP_T} I={C_I} ue8m0 row")
+        traffic = recorded_traffic(KERNEL_NAMES[DOMINANT], f"T={T} I={C_I} ue8m0 row")
         e2e = time_e2e(host, args.e2e_steps, dist)
         line = {
             "metric": METRIC, "value": round(agg["value"], 2), "unit": UNIT, "n_gpus": dist.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(agg["ms_per_step"], 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic (seeded generators; no dataset)", "config": step_config(),
+            "data": "synthetic (seeded generators; no dataset)", "config": step_config(T),
             "roofline": {"bound": "hbm", "kernel": KERNEL_NAMES[DOMINANT], "achieved": round(achieved, 1),
                          "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "peak_source": (f"{peak_kind}: MEASURED_PEAKS.json hbm_gbs (device copy bandwidth)"
@@ -690,7 +695,7 @@ def main(argv=None):
             "clocks": clocks.summary(*window),
         }
         if dist.rank == 0 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(host)
+            line["cpu_baseline"] = cpu_baseline(host, T)
         if dist.rank == 0:
             print(json.dumps(line), flush=True)
     finally:

@@ -42,6 +42,7 @@ EXPORTS = (
     "fp8q_f32_to_e4m3",
     "fp8q_status_string",
     "fp8q_version",
+    "fp8q_take_device_error",
 )
 
 _lib = None
@@ -74,6 +75,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.fp8q_status_string.restype = ctypes.c_char_p
     L.fp8q_version.argtypes = []
     L.fp8q_version.restype = ctypes.c_int
+    L.fp8q_take_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    L.fp8q_take_device_error.restype = ctypes.c_int
     _lib = L
     return L
 
@@ -108,6 +111,17 @@ def fp8q_status_string(status: int) -> str:
 
 def fp8q_version() -> int:
     return load().fp8q_version()
+
+
+FP8Q_DEVICE_ERR_TIMEOUT = 1
+
+
+def fp8q_take_device_error() -> int:
+    """Synchronise the device and return (and clear) the device error flags;
+    raises if the device cannot be read."""
+    flags = ctypes.c_uint32(0)
+    _check(load().fp8q_take_device_error(ctypes.byref(flags)), "fp8q_take_device_error")
+    return int(flags.value)
 
 
 # ------------------------------------------------ tensor-level calls ----

@@ -2,6 +2,7 @@
 // The contract of every entry point is stated in include/fp8q.h.
 #include "fp8q.h"
 #include "fp8q_kernels.cuh"
+#include "fp8q_rms.cuh"
 
 #include <cmath>
 #include <cstdint>
@@ -63,12 +64,13 @@ int sm_count()
 // scheduled while its predecessor on the stream drains, and waits for it
 // (griddepcontrol.wait) before touching global memory.
 template <typename... KArgs, typename... Args>
-cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t st, Args... args)
+cudaError_t launch_smem(void (*kernel)(KArgs...), dim3 grid, dim3 block, uint32_t smem, cudaStream_t st,
+                        Args... args)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
 #ifndef FP8Q_NO_PDL
     cudaLaunchAttribute attr[1];
@@ -78,6 +80,12 @@ cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t
     cfg.numAttrs = 1;
 #endif
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t st, Args... args)
+{
+    return launch_smem(kernel, grid, block, 0u, st, args...);
 }
 
 template <bool U, bool C, bool V>
@@ -97,23 +105,52 @@ cudaError_t launch_silu(const uint16_t *x, uint8_t *q, float *s, int64_t n, int6
                   dim3{unsigned(kCtaThreads)}, st, x, q, s, n, G, T, I, eps);
 }
 
-template <bool U, bool C, bool R, bool V, bool L>
-cudaError_t launch_rms(const uint16_t *x, uint16_t *res, const uint16_t *w, uint8_t *q, float *s,
-                       int64_t T, int H, int G, float eps, cudaStream_t st)
+// Dynamic shared memory above 48 KiB must be enabled per kernel and device.
+template <typename K>
+cudaError_t allow_smem(K kernel, uint32_t bytes)
 {
-    const int threads = ((4 * G + 31) / 32) * 32;
-    int64_t grid = T;
-    if (!L) {
-        // persistent: as many CTAs as are resident at once, at most one per row
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rms_quant_kernel<U, C, R, V, L>,
-                                                          threads, 0) != cudaSuccess || per_sm < 1)
-            per_sm = 1;
-        const int64_t resident = int64_t(per_sm) * sm_count();
-        grid = T < resident ? T : resident;
+    if (bytes <= 48u * 1024u)
+        return cudaSuccess;
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+}
+
+// Largest dynamic shared memory a CTA may use on sm_100-class parts.
+constexpr uint32_t kSmemPerCtaMax = 227u * 1024u;
+
+// Stages for rms_norm_per_block_quant: as many row stages (up to 8) as fit
+// three CTAs per SM, else two, else one CTA with whatever fits.
+int rms_stages(int H, bool res)
+{
+    for (uint32_t budget : {72u * 1024u, 110u * 1024u, kSmemPerCtaMax}) {
+        for (int S = kRmsMaxStages; S >= 1; --S) {
+            if (RmsSmem(H, res, S).total <= budget && (S >= 2 || budget == kSmemPerCtaMax))
+                return S;
+        }
     }
-    return launch(rms_quant_kernel<U, C, R, V, L>, dim3{unsigned(grid)}, dim3{unsigned(threads)}, st,
-                  x, res, w, q, s, T, H, G, eps);
+    return 0;
+}
+
+template <bool U, bool C, bool R>
+cudaError_t launch_rms(const uint16_t *x, uint16_t *res, const uint16_t *w, uint8_t *q, float *s,
+                       int T, int H, int G, float eps, cudaStream_t st)
+{
+    const int S = rms_stages(H, R);
+    if (S < 1)
+        return cudaErrorInvalidValue;
+    const uint32_t smem = RmsSmem(H, R, S).total;
+    auto kernel = rms_quant_kernel<U, C, R>;
+    cudaError_t e = allow_smem(kernel, smem);
+    if (e != cudaSuccess)
+        return e;
+    // one quad per group, up to 64 groups (longer rows loop over the groups)
+    const int threads = G >= kRmsMaxThreads / 4 ? kRmsMaxThreads : ((G + 7) / 8) * 32;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    const int64_t resident = int64_t(per_sm) * sm_count();
+    const int grid = int(T < resident ? T : resident);
+    return launch_smem(kernel, dim3{unsigned(grid)}, dim3{unsigned(threads)}, smem, st, x, res, w, q, s, T, H,
+                       G, eps, S);
 }
 
 }  // namespace
@@ -201,31 +238,25 @@ int fp8q_rms_norm_per_block_quant(const void *x, void *residual, const void *wei
         return FP8Q_ERR_INVALID_ARG;
     if (!aligned(weight, 16) || (residual && !aligned(residual, 16)))
         return FP8Q_ERR_MISALIGNED;
-    if (T > 0x7FFFFFFF)
+    if (T >= (int64_t(1) << 30))
         return FP8Q_ERR_UNSUPPORTED;
     const int G = int(H / kGroup);
-    const bool longrow = G > 64;   // rows above 8192 values: one row per CTA, up to 1024 threads
     auto st = static_cast<cudaStream_t>(stream);
     auto xp = static_cast<const uint16_t *>(x);
     auto rp = static_cast<uint16_t *>(residual);
     auto wp = static_cast<const uint16_t *>(weight);
     auto qp = static_cast<uint8_t *>(q);
     const bool col = scale_layout == FP8Q_SCALES_COL_MAJOR;
-    const bool v8 = aligned(x, 32) && aligned(q, 32) && aligned(weight, 32) && (!rp || aligned(rp, 32));
-    const int h = int(H);
+    const int t = int(T), h = int(H);
     cudaError_t e;
-#define FP8Q_RMS_L(U, C, R, V)                                                                   \
-    (longrow ? launch_rms<U, C, R, V, true>(xp, rp, wp, qp, scales, T, h, G, eps, st)           \
-             : launch_rms<U, C, R, V, false>(xp, rp, wp, qp, scales, T, h, G, eps, st))
-#define FP8Q_RMS_V(U, C, R) (v8 ? FP8Q_RMS_L(U, C, R, true) : FP8Q_RMS_L(U, C, R, false))
-#define FP8Q_RMS(U, C) (rp ? FP8Q_RMS_V(U, C, true) : FP8Q_RMS_V(U, C, false))
+#define FP8Q_RMS(U, C)                                                                           \
+    (rp ? launch_rms<U, C, true>(xp, rp, wp, qp, scales, t, h, G, eps, st)                      \
+        : launch_rms<U, C, false>(xp, rp, wp, qp, scales, t, h, G, eps, st))
     if (ue8m0)
         e = col ? FP8Q_RMS(true, true) : FP8Q_RMS(true, false);
     else
         e = col ? FP8Q_RMS(false, true) : FP8Q_RMS(false, false);
 #undef FP8Q_RMS
-#undef FP8Q_RMS_V
-#undef FP8Q_RMS_L
     return launch_status(e);
 }
 
@@ -259,6 +290,20 @@ const char *fp8q_status_string(int status)
     }
 }
 
-int fp8q_version(void) { return 200; }
+int fp8q_version(void) { return 300; }
+
+int fp8q_take_device_error(uint32_t *flags)
+{
+    if (!flags)
+        return FP8Q_ERR_INVALID_ARG;
+    uint32_t v = 0;
+    const uint32_t zero = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpyFromSymbol(&v, fp8q::g_device_error, sizeof v) != cudaSuccess ||
+        cudaMemcpyToSymbol(fp8q::g_device_error, &zero, sizeof zero) != cudaSuccess)
+        return FP8Q_ERR_CUDA;
+    *flags = v;
+    return FP8Q_OK;
+}
 
 }  // extern "C"

@@ -256,6 +256,65 @@ __device__ __forceinline__ float quotient(float x, float s, float r)
     return copysignf(__fmaf_rn(e, r, y), x);
 }
 
+// --------------------------------------------------------- packed fp32x2 ---
+//
+// add/sub/mul/fma .rn.f32x2 round each half exactly like the scalar
+// instruction; one packed instruction takes one issue slot for two values.
+
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0,%1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+// A bf16x2 word (value 2k in the low half) as packed fp32x2 (exact).
+__device__ __forceinline__ uint64_t f2_from_bf16x2(uint32_t w)
+{
+    return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// max(|a|, |b|, |c|) in one three-input instruction.
+__device__ __forceinline__ float absmax3(float m, float a, float b)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(m), "f"(fabsf(a)), "f"(fabsf(b)));
+    return r;
+}
+
 // --------------------------------------------------------------- e4m3 ---
 
 // Four fp32 -> four float8_e4m3fn codes (round to nearest even, saturate to
@@ -281,6 +340,39 @@ __device__ __forceinline__ void quant32(const float (&v)[32], float s, float r, 
     for (int k = 0; k < 8; ++k)
         c[k] = pack4_e4m3(quotient<UE8M0>(v[4 * k], s, r), quotient<UE8M0>(v[4 * k + 1], s, r),
                           quotient<UE8M0>(v[4 * k + 2], s, r), quotient<UE8M0>(v[4 * k + 3], s, r));
+}
+
+// Quantise 8 values (four packed pairs) with their group's scale s and
+// r = scale_recip(s) into 8 codes (c0: values 0-3, c1: values 4-7).
+template <bool UE8M0>
+__device__ __forceinline__ void quant8(const uint64_t (&v)[4], float s, float r, uint32_t &c0, uint32_t &c1)
+{
+    float q[8];
+    if (UE8M0) {
+        const uint64_t r2 = f2_pack(r, r);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            f2_unpack(f2_mul(v[k], r2), q[2 * k], q[2 * k + 1]);
+    } else {
+        // Markstein's correction (see quotient()) on signed values; the sign of
+        // the quotient, zero included, is the sign of v, put back at the end.
+        const uint64_t r2 = f2_pack(r, r), ns2 = f2_pack(-s, -s);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint64_t y = f2_mul(v[k], r2);
+            uint64_t e = f2_fma(y, ns2, v[k]);
+            y = f2_fma(e, r2, y);
+            e = f2_fma(y, ns2, v[k]);
+            y = f2_fma(e, r2, y);
+            float vl, vh;
+            f2_unpack(v[k], vl, vh);
+            f2_unpack(y, q[2 * k], q[2 * k + 1]);
+            q[2 * k] = copysignf(q[2 * k], vl);
+            q[2 * k + 1] = copysignf(q[2 * k + 1], vh);
+        }
+    }
+    c0 = pack4_e4m3(q[0], q[1], q[2], q[3]);
+    c1 = pack4_e4m3(q[4], q[5], q[6], q[7]);
 }
 
 }  // namespace fp8q

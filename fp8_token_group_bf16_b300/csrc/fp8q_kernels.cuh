@@ -56,13 +56,21 @@ __global__ void __launch_bounds__(kCtaThreads) group_quant_kernel(const uint16_t
 #pragma unroll
     for (int j = 0; j < GPT; ++j) {
         const int64_t gi = first + int64_t(j) * kGroupsPerCta;
-        float v[32];
-        unpack32(raw[j], v);
-        const float amax = quad_max(absmax32(v));
+        uint64_t v[16];
+        float m = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            v[k] = f2_from_bf16x2(raw[j][k]);
+            m = absmax3(m, bf_lo(raw[j][k]), bf_hi(raw[j][k]));
+        }
+        const float amax = quad_max(m);
         const float s = group_scale<UE8M0>(amax, eps);
         const float r = scale_recip<UE8M0>(s);
         uint32_t codes[8];
-        quant32<UE8M0>(v, s, r, codes);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            quant8<UE8M0>(*reinterpret_cast<const uint64_t(*)[4]>(&v[4 * i]), s, r, codes[2 * i],
+                          codes[2 * i + 1]);
         if (gi < n_groups) {
             st32<V8>(q + gi * kGroup + sub * kValsPerLane, codes);
             if (sub == 0) {
@@ -84,15 +92,43 @@ __global__ void __launch_bounds__(kCtaThreads) group_quant_kernel(const uint16_t
 // One output group per quad: output group gi = (t, g) reads the gate values
 // x[t, g*128 ...] and the up values x[t, I + g*128 ...] (64 bytes of each per
 // lane, both loads issued first).
+//
+// v = RN32(RN32(a / d) * b) with d = RN32(1 + expf(-a)).  The quotient is
+// formed from r = rcp.approx(d) with one residual correction,
+// q = q0 + RN32(a - q0 d) r, q0 = RN32(a r) (Newton-Raphson on the quotient;
+// the residual is exact by FMA), which is the correctly rounded a / d except
+// in rare cases where it is one ulp off, and is cheaper than IEEE division.
+// expf's argument is capped at 88 (e^88 < FLT_MAX) so that d stays finite:
+// for a below -88 the exact result is a negative number below 1e-36 (or -0),
+// whose code is a zero of the same sign either way.  Pairs of values go
+// through packed fp32x2 instructions.
 // --------------------------------------------------------------------------
-__device__ __forceinline__ float silu_mul(float a, float b)
+__device__ __forceinline__ float rcp_approx(float d)
 {
-    const float d = __fadd_rn(1.0f, expf(-a));
-    return __fmul_rn(__fdiv_rn(a, d), b);
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t silu_mul2(uint32_t aw, uint32_t bw)
+{
+    const uint64_t a = f2_from_bf16x2(aw), b = f2_from_bf16x2(bw);
+    float a0, a1;
+    f2_unpack(a, a0, a1);
+    const uint64_t e = f2_pack(expf(fminf(-a0, 88.0f)), expf(fminf(-a1, 88.0f)));
+    const uint64_t d = f2_add(f2_pack(1.0f, 1.0f), e);
+    const uint64_t nd = f2_sub(f2_pack(-1.0f, -1.0f), e);   // exactly -d
+    float d0, d1;
+    f2_unpack(d, d0, d1);
+    const uint64_t r = f2_pack(rcp_approx(d0), rcp_approx(d1));
+    const uint64_t q0 = f2_mul(a, r);
+    const uint64_t res = f2_fma(q0, nd, a);
+    const uint64_t q = f2_fma(res, r, q0);
+    return f2_mul(q, b);
 }
 
 template <bool UE8M0, bool COL, bool V8>
-__global__ void __launch_bounds__(kCtaThreads) silu_quant_kernel(const uint16_t *__restrict__ x,
+__global__ void __launch_bounds__(kCtaThreads, 3) silu_quant_kernel(const uint16_t *__restrict__ x,
                                                                  uint8_t *__restrict__ q,
                                                                  float *__restrict__ scales,
                                                                  int64_t n_groups, int64_t G,
@@ -110,133 +146,26 @@ __global__ void __launch_bounds__(kCtaThreads) silu_quant_kernel(const uint16_t 
     ld64_stream<V8>(pa, ra);
     ld64_stream<V8>(pa + I, rb);
 
-    float v[32];
+    uint64_t v[16];
+    float m = 0.0f;
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-        v[2 * k] = silu_mul(bf_lo(ra[k]), bf_lo(rb[k]));
-        v[2 * k + 1] = silu_mul(bf_hi(ra[k]), bf_hi(rb[k]));
+        v[k] = silu_mul2(ra[k], rb[k]);
+        float v0, v1;
+        f2_unpack(v[k], v0, v1);
+        m = absmax3(m, v0, v1);
     }
-    const float amax = quad_max(absmax32(v));
+    const float amax = quad_max(m);
     const float s = group_scale<UE8M0>(amax, eps);
     const float r = scale_recip<UE8M0>(s);
     uint32_t codes[8];
-    quant32<UE8M0>(v, s, r, codes);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        quant8<UE8M0>(*reinterpret_cast<const uint64_t(*)[4]>(&v[4 * i]), s, r, codes[2 * i], codes[2 * i + 1]);
     if (gi < n_groups) {
         st32<V8>(q + gi * kGroup + sub * kValsPerLane, codes);
         if (sub == 0)
             scales[COL ? g * T + t : gi] = s;
-    }
-}
-
-// --------------------------------------------------------------------------
-// rms_norm_per_block_quant
-//
-// A CTA of 4*G lanes (rounded up to whole warps) owns whole rows: quad g
-// holds group g of the row, 32 values per lane.  The row's sum of squares is
-// reduced per lane (two interleaved fma chains), per warp (butterfly) and
-// across warps through shared memory in warp order, so every lane gets the
-// same value.  Lanes past the end of the row (G not a multiple of 8) hold a
-// clamped copy of group G-1 and add nothing.
-//
-// Rows of up to 8192 values (<= 256 threads, !LONG): the CTA is persistent
-// (grid = resident CTAs, rows t = blockIdx.x + k*gridDim.x), keeps its slice
-// of the weight in registers across rows, and loads row t + gridDim.x while
-// it reduces and quantises row t.  Longer rows (LONG, <= 1024 threads) take
-// one row per CTA and read the weight after the reduction.
-// --------------------------------------------------------------------------
-template <bool RES, bool V8>
-__device__ __forceinline__ void load_row(const uint16_t *x, const uint16_t *residual, int64_t off,
-                                         uint32_t (&xr)[16], uint32_t (&rr)[16])
-{
-    ld64_stream<V8>(x + off, xr);
-    if (RES)
-        ld64_rw<V8>(residual + off, rr);
-}
-
-template <bool UE8M0, bool COL, bool RES, bool V8, bool LONG>
-__global__ void __launch_bounds__(LONG ? 1024 : 256) rms_quant_kernel(
-    const uint16_t *__restrict__ x, uint16_t *__restrict__ residual, const uint16_t *__restrict__ w,
-    uint8_t *__restrict__ q, float *__restrict__ scales, int64_t T, int H, int G, float eps)
-{
-    __shared__ float part[2][32];
-    const int sub = threadIdx.x & (kLanesPerGroup - 1);
-    const int g = threadIdx.x / kLanesPerGroup;
-    const int warp = threadIdx.x >> 5;
-    const int nwarps = blockDim.x >> 5;
-    const bool ok = g < G;
-    const int col = (ok ? g : G - 1) * kGroup + sub * kValsPerLane;   // clamped into the row
-
-    wait_for_producer();
-    allow_consumer_launch();
-    uint32_t wr[16];
-    if (!LONG)
-        ld64_keep<V8>(w + col, wr);
-
-    int64_t t = blockIdx.x;
-    uint32_t cx[16], cr[16];
-    load_row<RES, V8>(x, residual, t * H + col, cx, cr);
-
-    for (int it = 0; t < T; ++it, t += gridDim.x) {
-        uint32_t nx[16], nr[16];
-        const int64_t tn = t + gridDim.x;
-        if (!LONG && tn < T) {
-            load_row<RES, V8>(x, residual, tn * H + col, nx, nr);
-        } else {
-#pragma unroll
-            for (int k = 0; k < 16; ++k)
-                nx[k] = nr[k] = 0u;
-        }
-
-        if (RES) {
-            // z = bf16(x + r), written back to the residual, is what is normalised
-#pragma unroll
-            for (int k = 0; k < 16; ++k)
-                cx[k] = pack_bf16x2(__fadd_rn(bf_lo(cx[k]), bf_lo(cr[k])), __fadd_rn(bf_hi(cx[k]), bf_hi(cr[k])));
-            if (ok)
-                st64<V8>(residual + t * H + col, cx);
-        }
-
-        float ss0 = 0.0f, ss1 = 0.0f;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            ss0 = __fmaf_rn(bf_lo(cx[k]), bf_lo(cx[k]), ss0);
-            ss1 = __fmaf_rn(bf_hi(cx[k]), bf_hi(cx[k]), ss1);
-        }
-        const float ssw = warp_sum(ok ? __fadd_rn(ss0, ss1) : 0.0f);
-        if ((threadIdx.x & 31) == 0)
-            part[it & 1][warp] = ssw;
-        __syncthreads();
-        float tot = 0.0f;
-        for (int i = 0; i < nwarps; ++i)
-            tot = __fadd_rn(tot, part[it & 1][i]);
-
-        const float mean = __fdiv_rn(tot, float(H));
-        const float rstd = __fsqrt_rn(__fadd_rn(mean, eps));
-        const float inv = __frcp_rn(rstd);
-
-        if (LONG)
-            ld64_keep<V8>(w + col, wr);
-        float v[32];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            v[2 * k] = __fmul_rn(__fmul_rn(bf_lo(cx[k]), inv), bf_lo(wr[k]));
-            v[2 * k + 1] = __fmul_rn(__fmul_rn(bf_hi(cx[k]), inv), bf_hi(wr[k]));
-        }
-        const float amax = quad_max(absmax32(v));
-        const float s = group_scale<UE8M0>(amax, kScaleFloor);
-        const float r = scale_recip<UE8M0>(s);
-        uint32_t codes[8];
-        quant32<UE8M0>(v, s, r, codes);
-        if (ok) {
-            st32<V8>(q + t * H + col, codes);
-            if (sub == 0)
-                scales[COL ? int64_t(g) * T + t : t * G + g] = s;
-        }
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            cx[k] = nx[k];
-            cr[k] = nr[k];
-        }
     }
 }
 

@@ -96,11 +96,17 @@ FP8Q_API int fp8q_per_token_group_quant(const void *x, void *q, float *scales, i
  *   weight    bf16 [H], read.
  *   q, scales as for per_token_group_quant (scale floor 1e-10).
  *   eps       the RMSNorm variance epsilon (e.g. 1e-6), finite and >= 0.
- * Per row: ss = sum z_h^2 (fp32, tree order); inv = RN32(1/RN32(sqrt(
+ * Per row: ss = sum z_h^2 rounded once to fp32 (the GPU adds the squares
+ * with error-free transformations, so ss is the exact sum rounded once unless
+ * squares underflow fp32, |z| < ~1e-19); inv = RN32(1/RN32(sqrt(
  * RN32(RN32(ss/H) + eps)))); v_h = RN32(RN32(z_h * inv) * w_h); then the
- * group quantisation of v.  Only the summation order of ss differs from a
- * sequential sum, so scales agree with it to a few ulps and codes to one
- * e4m3 step on rare elements.  H <= FP8Q_RMS_MAX_H.
+ * group quantisation of v.  Outside the underflow case the result is
+ * therefore the same, bit for bit, as a sequential evaluation of these steps
+ * with the sum carried in double precision.  H <= FP8Q_RMS_MAX_H,
+ * T < 2^30.  Rows are staged in shared memory by bulk asynchronous copies;
+ * a kernel that waited more than about a second for one gives up, leaves the
+ * remaining rows unwritten and sets FP8Q_DEVICE_ERR_TIMEOUT (see
+ * fp8q_take_device_error).
  */
 FP8Q_API int fp8q_rms_norm_per_block_quant(const void *x, void *residual, const void *weight, void *q,
                                   float *scales, int64_t T, int64_t H, int32_t group_size,
@@ -127,6 +133,17 @@ FP8Q_API int fp8q_silu_and_mul_per_block_quant(const void *x, void *q, float *sc
  * aligned.  Exposed so the rounding can be checked on its own.
  */
 FP8Q_API int fp8q_f32_to_e4m3(const float *v, void *out, int64_t n, void *stream);
+
+/*
+ * Device-side error flags, set by a kernel that stopped early (it gave up
+ * waiting on a shared-memory barrier after about one second).  Bits:
+ * FP8Q_DEVICE_ERR_TIMEOUT.  The call synchronises the current device, stores
+ * the flags raised since the previous call into *flags, and clears them.
+ * Returns FP8Q_ERR_INVALID_ARG for a NULL flags, FP8Q_ERR_CUDA if the device
+ * cannot be synchronised or read (for example after a fault).
+ */
+#define FP8Q_DEVICE_ERR_TIMEOUT 1u
+FP8Q_API int fp8q_take_device_error(uint32_t *flags);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 FP8Q_API const char *fp8q_status_string(int status);

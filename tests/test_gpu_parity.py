@@ -274,3 +274,40 @@ def test_silu_extreme_gates():
     xb = inputs.bits(inputs.bf16(torch.cat([a, b], dim=1)))
     for ue8m0, col in VARIANTS:
         _check_silu(xb, ue8m0, col, what="silu extreme gates")
+
+
+# ------------------------------------ op B: the exact sum of squares ----
+
+
+@pytest.mark.parametrize("residual", [False, True], ids=["plain", "residual"])
+@pytest.mark.parametrize("ue8m0,col", VARIANTS, ids=VID)
+def test_rms_bit_exact(residual, ue8m0, col):
+    """The GPU adds the squares without rounding error and rounds once, so
+    away from fp32 underflow op B equals the oracle bit for bit."""
+    x, w, r = inputs.rms_input(256, 4096)
+    xb, wb, rb = inputs.bits(x), inputs.bits(w), inputs.bits(r) if residual else None
+    q, s, rout = gpu_rms(xb, wb, rb, ue8m0, col)
+    qr, sr, _, _, ror = oracle.rms_norm_per_block_quant(xb, wb, rb, ue8m0=ue8m0, col_major=col)
+    assert_exact(q, s, qr, to_tg(sr, col), f"rms residual={residual}")
+    if residual:
+        assert np.array_equal(rout, ror)
+
+
+@pytest.mark.parametrize("T,H", [(3, 24576), (512, 5120), (37, 1152), (2, 32768)])
+def test_rms_bit_exact_shapes(T, H):
+    x = inputs.lognormal_channel_input(T, H, 6000 + T)
+    w = inputs.rms_weight(H)
+    xb, wb = inputs.bits(x), inputs.bits(w)
+    q, s, _ = gpu_rms(xb, wb, None, True, False)
+    qr, sr, _, _, _ = oracle.rms_norm_per_block_quant(xb, wb, None, ue8m0=True)
+    assert_exact(q, s, qr, sr, f"rms T={T} H={H}")
+
+
+def test_no_device_error_raised():
+    import fp8_token_group_bf16_b300 as fq
+
+    x, w, r = inputs.rms_input(64, 5120)
+    gpu_rms(inputs.bits(x), inputs.bits(w), inputs.bits(r), True, True)
+    gpu_silu(inputs.bits(inputs.silu_input(8, 1024)), True, False)
+    gpu_group_quant(inputs.bits(inputs.small_group_quant_input()))
+    assert fq.fp8q_take_device_error() == 0
