@@ -33,6 +33,7 @@ FP8Q_ERR_CUDA = 4
 FP8Q_SCALES_ROW_MAJOR = 0
 FP8Q_SCALES_COL_MAJOR = 1
 FP8Q_RMS_MAX_H = 32768
+FP8Q_RMS_MAX_H_RESIDUAL = 16384
 GROUP = 128
 
 EXPORTS = (

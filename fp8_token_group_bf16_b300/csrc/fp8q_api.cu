@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <mutex>
 
 namespace {
 
@@ -88,6 +89,63 @@ cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t
     return launch_smem(kernel, grid, block, 0u, st, args...);
 }
 
+// Launch shapes depend only on the device, the kernel and the row length;
+// they are computed once (occupancy queries cost microseconds of host time)
+// and remembered in a small table shared by all host threads.
+struct ShapeCache {
+    struct Entry {
+        int dev;
+        const void *fn;
+        int H;
+        int a, b, c;
+    };
+    static constexpr int kEntries = 64;
+    std::mutex mu;
+    Entry e[kEntries];
+    int n = 0, next = 0;
+
+    bool find(int dev, const void *fn, int H, int &a, int &b, int &c)
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < n; ++i)
+            if (e[i].dev == dev && e[i].fn == fn && e[i].H == H) {
+                a = e[i].a, b = e[i].b, c = e[i].c;
+                return true;
+            }
+        return false;
+    }
+    void put(int dev, const void *fn, int H, int a, int b, int c)
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        const int i = n < kEntries ? n++ : (next++ % kEntries);
+        e[i] = Entry{dev, fn, H, a, b, c};
+    }
+};
+
+ShapeCache &shape_cache()
+{
+    static ShapeCache cache;
+    return cache;
+}
+
+int current_device()
+{
+    int dev = 0;
+    return cudaGetDevice(&dev) == cudaSuccess ? dev : -1;
+}
+
+// Dynamic shared memory above 48 KiB must be enabled per kernel and device.
+template <typename K>
+cudaError_t allow_smem(K kernel, uint32_t bytes)
+{
+    if (bytes <= 48u * 1024u)
+        return cudaSuccess;
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+}
+
+// Largest dynamic shared memory a CTA may use on sm_100-class parts.
+constexpr uint32_t kSmemPerCtaMax = 227u * 1024u;
+
 template <bool U, bool C, bool V>
 cudaError_t launch_group(const uint16_t *x, uint8_t *q, float *s, int64_t n, int64_t G, int64_t T,
                          float eps, cudaStream_t st)
@@ -105,52 +163,104 @@ cudaError_t launch_silu(const uint16_t *x, uint8_t *q, float *s, int64_t n, int6
                   dim3{unsigned(kCtaThreads)}, st, x, q, s, n, G, T, I, eps);
 }
 
-// Dynamic shared memory above 48 KiB must be enabled per kernel and device.
-template <typename K>
-cudaError_t allow_smem(K kernel, uint32_t bytes)
-{
-    if (bytes <= 48u * 1024u)
-        return cudaSuccess;
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
-}
-
-// Largest dynamic shared memory a CTA may use on sm_100-class parts.
-constexpr uint32_t kSmemPerCtaMax = 227u * 1024u;
-
-// Stages for rms_norm_per_block_quant: as many row stages (up to 8) as fit
-// three CTAs per SM, else two, else one CTA with whatever fits.
-int rms_stages(int H, bool res)
+// rms_norm_per_block_quant, one CTA per row: as many row stages (up to 8) as
+// fit three CTAs per SM, else two, else one CTA with whatever fits.
+int rms_cta_stages(int H, bool res)
 {
     for (uint32_t budget : {72u * 1024u, 110u * 1024u, kSmemPerCtaMax}) {
         for (int S = kRmsMaxStages; S >= 1; --S) {
-            if (RmsSmem(H, res, S).total <= budget && (S >= 2 || budget == kSmemPerCtaMax))
+            if (RmsCtaSmem(H, res, S).total <= budget && (S >= 2 || budget == kSmemPerCtaMax))
                 return S;
         }
     }
     return 0;
 }
 
+// one quad per group, up to 64 groups (longer rows loop over the groups)
+int rms_cta_threads(int G) { return G >= kRmsMaxThreads / 4 ? kRmsMaxThreads : ((G + 7) / 8) * 32; }
+
 template <bool U, bool C, bool R>
+cudaError_t launch_rms_cta(const uint16_t *x, uint16_t *res, const uint16_t *w, uint8_t *q, float *s,
+                           int T, int H, int G, float eps, cudaStream_t st)
+{
+    auto kernel = rms_cta_kernel<U, C, R>;
+    const int dev = current_device();
+    int S = 0, per_sm = 0, unused = 0;
+    if (!shape_cache().find(dev, reinterpret_cast<const void *>(kernel), H, S, per_sm, unused)) {
+        S = rms_cta_stages(H, R);
+        if (S < 1)
+            return cudaErrorInvalidValue;
+        const uint32_t smem = RmsCtaSmem(H, R, S).total;
+        // the cap is raised once to the largest shape; each launch asks for its own size
+        cudaError_t e = allow_smem(kernel, kSmemPerCtaMax);
+        if (e != cudaSuccess)
+            return e;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, rms_cta_threads(G), smem) != cudaSuccess ||
+            per_sm < 1) {
+            cudaGetLastError();
+            per_sm = 1;
+        }
+        shape_cache().put(dev, reinterpret_cast<const void *>(kernel), H, S, per_sm, 0);
+    }
+    const uint32_t smem = RmsCtaSmem(H, R, S).total;
+    const int64_t resident = int64_t(per_sm) * sm_count();
+    const int grid = int(T < resident ? T : resident);
+    return launch_smem(kernel, dim3{unsigned(grid)}, dim3{unsigned(rms_cta_threads(G))}, smem, st, x, res, w, q, s,
+                       T, H, G, eps, S);
+}
+
+// rms_norm_per_block_quant, one warp per row, two passes (the second from
+// L2): resident CTAs of 8 warps, no more than there are rows for.
+template <int NG, bool U, bool C, bool R, bool V>
+cudaError_t launch_rms_l2(const uint16_t *x, uint16_t *res, const uint16_t *w, uint8_t *q, float *s, int T,
+                          int H, int G, float eps, cudaStream_t st)
+{
+    auto kernel = rms_l2_kernel<NG, U, C, R, V>;
+    constexpr int kWarps = kRmsMaxThreads / 32;
+    const uint32_t smem = uint32_t(H) * 4u;   // the fp32 weight table
+    const int dev = current_device();
+    int per_sm = 0, unused_a = 0, unused_b = 0;
+    if (!shape_cache().find(dev, reinterpret_cast<const void *>(kernel), H, per_sm, unused_a, unused_b)) {
+        cudaError_t e = allow_smem(kernel, kSmemPerCtaMax);
+        if (e != cudaSuccess)
+            return e;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kRmsMaxThreads, smem) != cudaSuccess ||
+            per_sm < 1) {
+            cudaGetLastError();
+            per_sm = 1;
+        }
+        shape_cache().put(dev, reinterpret_cast<const void *>(kernel), H, per_sm, 0, 0);
+    }
+    int64_t grid = int64_t(per_sm) * sm_count();
+    const int64_t need = (T + kWarps - 1) / kWarps;
+    if (need < grid)
+        grid = need;
+    return launch_smem(kernel, dim3{unsigned(grid)}, dim3{unsigned(kRmsMaxThreads)}, smem, st, x, res, w, q, s, T,
+                       H, G, eps);
+}
+
+// Rows per launch from which the warp-per-row kernel takes over: below it a
+// row's latency, not the bytes, decides, and a CTA spreads a row over up to
+// 64 quads.
+constexpr int kRmsWarpMinRows = 1024;
+
+template <bool U, bool C, bool R, bool V>
 cudaError_t launch_rms(const uint16_t *x, uint16_t *res, const uint16_t *w, uint8_t *q, float *s,
                        int T, int H, int G, float eps, cudaStream_t st)
 {
-    const int S = rms_stages(H, R);
-    if (S < 1)
-        return cudaErrorInvalidValue;
-    const uint32_t smem = RmsSmem(H, R, S).total;
-    auto kernel = rms_quant_kernel<U, C, R>;
-    cudaError_t e = allow_smem(kernel, smem);
-    if (e != cudaSuccess)
-        return e;
-    // one quad per group, up to 64 groups (longer rows loop over the groups)
-    const int threads = G >= kRmsMaxThreads / 4 ? kRmsMaxThreads : ((G + 7) / 8) * 32;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess || per_sm < 1)
-        per_sm = 1;
-    const int64_t resident = int64_t(per_sm) * sm_count();
-    const int grid = int(T < resident ? T : resident);
-    return launch_smem(kernel, dim3{unsigned(grid)}, dim3{unsigned(threads)}, smem, st, x, res, w, q, s, T, H,
-                       G, eps, S);
+    if (T >= kRmsWarpMinRows && G <= 8 * kL2MaxGroups) {
+        switch ((G + 7) / 8) {
+        case 1: return launch_rms_l2<1, U, C, R, V>(x, res, w, q, s, T, H, G, eps, st);
+        case 2: return launch_rms_l2<2, U, C, R, V>(x, res, w, q, s, T, H, G, eps, st);
+        case 3: return launch_rms_l2<3, U, C, R, V>(x, res, w, q, s, T, H, G, eps, st);
+        case 4: return launch_rms_l2<4, U, C, R, V>(x, res, w, q, s, T, H, G, eps, st);
+        case 5: return launch_rms_l2<5, U, C, R, V>(x, res, w, q, s, T, H, G, eps, st);
+        case 6: return launch_rms_l2<6, U, C, R, V>(x, res, w, q, s, T, H, G, eps, st);
+        case 7: return launch_rms_l2<7, U, C, R, V>(x, res, w, q, s, T, H, G, eps, st);
+        default: return launch_rms_l2<8, U, C, R, V>(x, res, w, q, s, T, H, G, eps, st);
+        }
+    }
+    return launch_rms_cta<U, C, R>(x, res, w, q, s, T, H, G, eps, st);
 }
 
 }  // namespace
@@ -230,7 +340,7 @@ int fp8q_rms_norm_per_block_quant(const void *x, void *residual, const void *wei
         return rc;
     if (!std::isfinite(eps) || eps < 0.0f)
         return FP8Q_ERR_INVALID_ARG;
-    if (H > FP8Q_RMS_MAX_H)
+    if (H > (residual ? FP8Q_RMS_MAX_H_RESIDUAL : FP8Q_RMS_MAX_H))
         return FP8Q_ERR_UNSUPPORTED;
     if (T == 0)
         return FP8Q_OK;
@@ -249,14 +359,17 @@ int fp8q_rms_norm_per_block_quant(const void *x, void *residual, const void *wei
     const bool col = scale_layout == FP8Q_SCALES_COL_MAJOR;
     const int t = int(T), h = int(H);
     cudaError_t e;
-#define FP8Q_RMS(U, C)                                                                           \
-    (rp ? launch_rms<U, C, true>(xp, rp, wp, qp, scales, t, h, G, eps, st)                      \
-        : launch_rms<U, C, false>(xp, rp, wp, qp, scales, t, h, G, eps, st))
+    const bool v8 = aligned(x, 32) && aligned(q, 32) && (!rp || aligned(rp, 32));
+#define FP8Q_RMS_V(U, C, R)                                                                      \
+    (v8 ? launch_rms<U, C, R, true>(xp, rp, wp, qp, scales, t, h, G, eps, st)                   \
+        : launch_rms<U, C, R, false>(xp, rp, wp, qp, scales, t, h, G, eps, st))
+#define FP8Q_RMS(U, C) (rp ? FP8Q_RMS_V(U, C, true) : FP8Q_RMS_V(U, C, false))
     if (ue8m0)
         e = col ? FP8Q_RMS(true, true) : FP8Q_RMS(true, false);
     else
         e = col ? FP8Q_RMS(false, true) : FP8Q_RMS(false, false);
 #undef FP8Q_RMS
+#undef FP8Q_RMS_V
     return launch_status(e);
 }
 

@@ -1,14 +1,12 @@
-// Device helpers shared by the three quantisation kernels: vector memory
-// access, dependent-launch control, bf16 unpacking, the group reduction, the
-// group scale, the correctly rounded quotient and the packed e4m3 conversion.
+// Device helpers shared by the quantisation kernels: dependent-launch
+// control, bf16 unpacking, the quad reduction, the group scale, packed fp32x2
+// arithmetic, the correctly rounded quotient and the packed e4m3 conversion.
 //
 // A group is 128 consecutive values of one token row (the Block_FP8 "1x128
 // activation scaling" of "Helion：用自动调优改进 vLLM 推理", section Scope).
-// It is held by a quad of 4 consecutive lanes, 32 values per lane (64 bytes of
-// bf16: two 256-bit loads on sm_100+ parts, four 128-bit loads when the
-// buffers are only 16-byte aligned), so a warp covers 8 groups.  The per-group
-// work (two shuffles, the scale, its reciprocal) is then spread over 32
-// values per lane.
+// It is held by a quad of 4 consecutive lanes, 32 values per lane, so a warp
+// covers 8 groups.  The per-group work (two shuffles, the scale, its
+// reciprocal) is then spread over 32 values per lane.
 #pragma once
 
 #include <cstdint>
@@ -41,7 +39,8 @@ constexpr float kScaleFloor = 1e-10f;
                  : "l"(p)                                                                     \
                  : "memory")
 
-// 64 bytes read once (streamed input): read-only path, L2 evict-first.
+// 64 bytes read once (streamed input): read-only path, L2 evict-first (the
+// eviction hint exists for 256-bit loads only).
 template <bool V8>
 __device__ __forceinline__ void ld64_stream(const void *p, uint32_t (&w)[16])
 {
@@ -56,18 +55,19 @@ __device__ __forceinline__ void ld64_stream(const void *p, uint32_t (&w)[16])
     }
 }
 
-// 64 bytes every CTA re-reads (the RMSNorm weight): read-only, kept in L2.
+// 64 bytes that will be read again soon (from L2): read-only path, no L1
+// allocation, default L2 policy.
 template <bool V8>
 __device__ __forceinline__ void ld64_keep(const void *p, uint32_t (&w)[16])
 {
     const char *c = static_cast<const char *>(p);
     if (V8) {
-        FP8Q_LD8(".nc.L2::evict_last", c, w, 0);
-        FP8Q_LD8(".nc.L2::evict_last", c + 32, w, 8);
+        FP8Q_LD8(".nc.L1::no_allocate", c, w, 0);
+        FP8Q_LD8(".nc.L1::no_allocate", c + 32, w, 8);
     } else {
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-            FP8Q_LD4(".nc", c + 16 * k, w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+            FP8Q_LD4(".nc.L1::no_allocate", c + 16 * k, w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
     }
 }
 
@@ -77,8 +77,8 @@ __device__ __forceinline__ void ld64_rw(const void *p, uint32_t (&w)[16])
 {
     const char *c = static_cast<const char *>(p);
     if (V8) {
-        FP8Q_LD8(".L1::no_allocate.L2::evict_first", c, w, 0);
-        FP8Q_LD8(".L1::no_allocate.L2::evict_first", c + 32, w, 8);
+        FP8Q_LD8(".L1::no_allocate", c, w, 0);
+        FP8Q_LD8(".L1::no_allocate", c + 32, w, 8);
     } else {
 #pragma unroll
         for (int k = 0; k < 4; ++k)
@@ -86,6 +86,7 @@ __device__ __forceinline__ void ld64_rw(const void *p, uint32_t (&w)[16])
     }
 }
 
+// 64 bytes (32 bf16 values) to global memory.
 template <bool V8>
 __device__ __forceinline__ void st64(void *p, const uint32_t (&w)[16])
 {
@@ -106,7 +107,7 @@ __device__ __forceinline__ void st64(void *p, const uint32_t (&w)[16])
     }
 }
 
-// 32 e4m3 codes (32 bytes).
+// 32 bytes (32 codes) to global memory.
 template <bool V8>
 __device__ __forceinline__ void st32(void *p, const uint32_t (&w)[8])
 {
@@ -154,15 +155,6 @@ __device__ __forceinline__ void allow_consumer_launch()
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-__device__ __forceinline__ void unpack32(const uint32_t (&w)[16], float (&f)[32])
-{
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        f[2 * k] = bf_lo(w[k]);
-        f[2 * k + 1] = bf_hi(w[k]);
-    }
-}
-
 // Two fp32 -> packed bf16x2 with round to nearest even (lo at the lower address).
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
@@ -180,25 +172,6 @@ __device__ __forceinline__ float quad_max(float m)
     m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
     m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
     return m;
-}
-
-__device__ __forceinline__ float warp_sum(float s)
-{
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1)
-        s = __fadd_rn(s, __shfl_xor_sync(0xFFFFFFFFu, s, o));
-    return s;
-}
-
-__device__ __forceinline__ float absmax32(const float (&v)[32])
-{
-    float m0 = fabsf(v[0]), m1 = fabsf(v[1]);
-#pragma unroll
-    for (int k = 2; k < 32; k += 2) {
-        m0 = fmaxf(m0, fabsf(v[k]));
-        m1 = fmaxf(m1, fabsf(v[k + 1]));
-    }
-    return fmaxf(m0, m1);
 }
 
 // ------------------------------------------------------------ scale -----
@@ -228,32 +201,6 @@ __device__ __forceinline__ float scale_recip(float s)
     if (UE8M0)
         return __uint_as_float(0x7F000000u - (__float_as_uint(s) & 0x7F800000u));
     return __frcp_rn(s);
-}
-
-// Correctly rounded x / s, given r = RN32(1/s).
-//
-// Power-of-two s: r is exactly 1/s, so one multiply is the exact quotient
-// rounded once (its sign, zero included, is the sign of x).  Otherwise, on
-// |x|: y0 = RN(|x| r) is within 1.5 ulp of |x|/s; one residual step
-// y1 = RN(y0 + RN(|x| - s y0) r) makes it faithful; a second step with the
-// exact residual |x| - s y1 (an FMA) then yields RN32(|x|/s) by Markstein's
-// theorem (P. Markstein, "Computation of elementary functions on the IBM
-// RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990: a faithful
-// quotient corrected with a correctly rounded reciprocal and an exact FMA
-// residual is the correctly rounded quotient, barring underflow).  Underflow
-// only happens for quotients far below 2^-10, whose e4m3 code is zero either
-// way.  The sign of x, zero included, is put back last.
-template <bool POW2>
-__device__ __forceinline__ float quotient(float x, float s, float r)
-{
-    if (POW2)
-        return __fmul_rn(x, r);
-    const float ax = fabsf(x);
-    float y = __fmul_rn(ax, r);
-    float e = __fmaf_rn(-y, s, ax);
-    y = __fmaf_rn(e, r, y);
-    e = __fmaf_rn(-y, s, ax);
-    return copysignf(__fmaf_rn(e, r, y), x);
 }
 
 // --------------------------------------------------------- packed fp32x2 ---
@@ -332,18 +279,22 @@ __device__ __forceinline__ uint32_t pack4_e4m3(float a0, float a1, float a2, flo
     return r;
 }
 
-// Quantise the 32 values of a lane with its group's scale into 32 codes.
-template <bool UE8M0>
-__device__ __forceinline__ void quant32(const float (&v)[32], float s, float r, uint32_t (&c)[8])
-{
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        c[k] = pack4_e4m3(quotient<UE8M0>(v[4 * k], s, r), quotient<UE8M0>(v[4 * k + 1], s, r),
-                          quotient<UE8M0>(v[4 * k + 2], s, r), quotient<UE8M0>(v[4 * k + 3], s, r));
-}
-
 // Quantise 8 values (four packed pairs) with their group's scale s and
-// r = scale_recip(s) into 8 codes (c0: values 0-3, c1: values 4-7).
+// r = scale_recip(s) into 8 codes (c0: values 0-3, c1: values 4-7): each
+// code is e4m3(RN32(v / s)), the quotient correctly rounded.
+//
+// Power-of-two s (UE8M0): r is exactly 1/s, so one multiply is the exact
+// quotient rounded once (its sign, zero included, is the sign of v).
+// Otherwise: y0 = RN(v r) is within 1.5 ulp of v/s; one residual step
+// y1 = RN(y0 + RN(v - s y0) r) makes it faithful; a second step with the
+// exact residual v - s y1 (an FMA) then yields RN32(v/s) by Markstein's
+// theorem (P. Markstein, "Computation of elementary functions on the IBM
+// RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990: a faithful
+// quotient corrected with a correctly rounded reciprocal and an exact FMA
+// residual is the correctly rounded quotient, barring underflow).  Underflow
+// only happens for quotients far below 2^-10, whose e4m3 code is zero either
+// way.  Rounding to nearest is symmetric, so the steps run on signed values;
+// the sign of v, which a zero quotient can lose, is put back last.
 template <bool UE8M0>
 __device__ __forceinline__ void quant8(const uint64_t (&v)[4], float s, float r, uint32_t &c0, uint32_t &c1)
 {
@@ -354,8 +305,6 @@ __device__ __forceinline__ void quant8(const uint64_t (&v)[4], float s, float r,
         for (int k = 0; k < 4; ++k)
             f2_unpack(f2_mul(v[k], r2), q[2 * k], q[2 * k + 1]);
     } else {
-        // Markstein's correction (see quotient()) on signed values; the sign of
-        // the quotient, zero included, is the sign of v, put back at the end.
         const uint64_t r2 = f2_pack(r, r), ns2 = f2_pack(-s, -s);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {

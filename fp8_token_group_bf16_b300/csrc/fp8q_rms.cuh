@@ -1,28 +1,33 @@
 // rms_norm_per_block_quant for sm_103a: token rows staged in shared memory by
-// bulk asynchronous copies, an error-free row sum of squares, then the group
-// quantisation of the normalised row.
+// bulk asynchronous copies (TMA), an error-free row sum of squares, then the
+// group quantisation of the normalised row.
 //
-// One CTA works through rows t = blockIdx.x, blockIdx.x + gridDim.x, ...
-// (persistent: the grid is the number of CTAs resident at once).  Shared
-// memory holds S row stages, the weight, S + 1 mbarriers and the reduction
-// scratch.  Thread 0 keeps S - 1 rows in flight ahead of the row being
-// processed: each row (and its residual row) arrives with one bulk copy that
-// completes a stage barrier; the weight arrives once per CTA.
+// Two kernels share the per-row arithmetic below:
+//
+//  * rms_l2_kernel (many rows of up to 8192 values): a warp owns whole rows
+//    and reads each row twice, from HBM into registers for the sum of
+//    squares and from L2 for the quantisation (details at the kernel).
+//  * rms_cta_kernel (few rows, decode sizes, and longer rows): a CTA of one
+//    quad per group owns a row, so a row's work is spread over up to 64
+//    quads; the row is staged in shared memory by bulk asynchronous copies
+//    (TMA), the quads' partial sums meet in shared memory, and thread 0 keeps
+//    S - 1 rows in flight.
 //
 // Per row:
 //   pass 1  every quad of lanes takes a 128-value group (32 values a lane)
-//           from shared memory; with a residual, z = bf16(x + r) is written
-//           back to the stage and to the residual tensor; each lane sums its
-//           squares without rounding error (below), the quads' partial sums
-//           go to shared memory;
-//   warp 0  adds the partial sums (still without error), rounds once, and
-//           forms inv = 1 / sqrt(ss / H + eps);
+//           from its stage; with a residual, z = bf16(x + r) is written back
+//           to the stage and to the residual tensor; each lane sums its
+//           squares without rounding error (below) and the partial sums are
+//           combined, still without error, and rounded once: ss;
+//           inv = 1 / sqrt(ss / H + eps);
 //   pass 2  every quad reads its group again with the weight, v = (z inv) w,
 //           group amax, scale, codes, stores.
 // Reads of a lane's 64 bytes are rotated by (lane >> 1) & 3 sixteen-byte
 // pieces, so the 32 lanes of a warp hit all 32 banks evenly (four wavefronts
 // per 512 bytes); codes are stored in the same rotated order, eight bytes at
-// a time, to their own places.
+// a time, to their own places.  The weight is converted to fp32 once per CTA
+// into a table whose 16-byte units are XOR-swizzled so that the same rotated
+// reads of it are conflict-free as well.
 //
 // Sum of squares.  A lane seeds two accumulators with pm = the largest square
 // among its 32 values and adds the squares (each exact in fp32: a bf16 value
@@ -43,64 +48,308 @@ namespace fp8q {
 constexpr int kRmsMaxThreads = 256;
 constexpr int kRmsMaxStages = 8;
 
-// Byte offsets of the pieces of dynamic shared memory.
-struct RmsSmem {
-    uint32_t stage_bytes, stages, w_off, bar_off, red_off, inv_off, total;
+// Squares of one lane's 32 values (16 bf16x2 words), summed exactly:
+// returns (hi, lo) with hi + lo equal to the sum up to lo's own rounding.
+// Four accumulators (two packed pairs: even and odd words) shorten the
+// dependency chains.
+__device__ __forceinline__ void lane_sumsq(const uint32_t (&w)[16], float &hi, float &lo)
+{
+    float m0 = 0.0f, m1 = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 16; k += 2) {
+        m0 = absmax3(m0, bf_lo(w[k]), bf_hi(w[k]));
+        m1 = absmax3(m1, bf_lo(w[k + 1]), bf_hi(w[k + 1]));
+    }
+    const float m = fmaxf(m0, m1);
+    const float pm = __fmul_rn(m, m);
+    uint64_t s[2] = {f2_pack(pm, pm), f2_pack(pm, pm)};
+    uint64_t c[2] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f)};
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const int a = k & 1;
+        const uint64_t z = f2_from_bf16x2(w[k]);
+        const uint64_t p = f2_mul(z, z);
+        const uint64_t t = f2_add(s[a], p);
+        c[a] = f2_add(c[a], f2_sub(p, f2_sub(t, s[a])));   // Fast2Sum error, |s| >= |p|
+        s[a] = t;
+    }
+    float sv[4], cv[4];
+    f2_unpack(s[0], sv[0], sv[1]);
+    f2_unpack(s[1], sv[2], sv[3]);
+    f2_unpack(c[0], cv[0], cv[1]);
+    f2_unpack(c[1], cv[2], cv[3]);
+    const float inf = __int_as_float(0x7F800000);
+    if (!(sv[0] < inf && sv[1] < inf && sv[2] < inf && sv[3] < inf)) {   // the squares overflow fp32:
+        hi = inf;                                                         // so does the row sum
+        lo = 0.0f;
+        return;
+    }
+    // each accumulator minus its seed is exact; combine the four without error
+    float h01, e01, h23, e23;
+    two_sum(__fsub_rn(sv[0], pm), __fsub_rn(sv[1], pm), h01, e01);
+    two_sum(__fsub_rn(sv[2], pm), __fsub_rn(sv[3], pm), h23, e23);
+    float e;
+    two_sum(h01, h23, hi, e);
+    lo = __fadd_rn(__fadd_rn(__fadd_rn(cv[0], cv[1]), __fadd_rn(cv[2], cv[3])), __fadd_rn(__fadd_rn(e01, e23), e));
+}
 
-    __host__ __device__ RmsSmem(int H, bool res, int S)
+__device__ __forceinline__ float rms_inv(float hi, float lo, int H, float eps)
+{
+    const float ss = __fadd_rn(hi, lo);
+    return __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(ss, float(H)), eps)));
+}
+
+// ------------------------------------------------------- fp32 weight table ---
+//
+// Value v of the weight lives in line v / 32 (128 bytes: the 32 values one
+// lane of one quad handles), 16-byte unit (2k + h) ^ swz(line) with
+// k = (v % 32) / 8 (the lane's rotated piece) and h = (v % 8) / 4.
+
+__device__ __forceinline__ uint32_t w_swizzle(uint32_t line) { return (((line >> 3) & 3u) << 1) | (line & 1u); }
+
+// All threads of the CTA; the caller synchronises before the first read.
+__device__ __forceinline__ void fill_weight_table(const uint16_t *__restrict__ w, int H, uint32_t wsm)
+{
+    for (int c = threadIdx.x; c < H / 8; c += blockDim.x) {
+        uint32_t p[4];
+        FP8Q_LD4(".nc", w + 8 * c, p[0], p[1], p[2], p[3]);
+        const uint32_t line = uint32_t(c) >> 2, k = uint32_t(c) & 3u, swz = w_swizzle(line);
+        const uint32_t lo[4] = {p[0] << 16, p[0] & 0xFFFF0000u, p[1] << 16, p[1] & 0xFFFF0000u};
+        const uint32_t hi[4] = {p[2] << 16, p[2] & 0xFFFF0000u, p[3] << 16, p[3] & 0xFFFF0000u};
+        sts128(wsm + line * 128u + ((2u * k) ^ swz) * 16u, lo);
+        sts128(wsm + line * 128u + ((2u * k + 1u) ^ swz) * 16u, hi);
+    }
+}
+
+// ------------------------------------------------------- per-group work ---
+
+// Pass 1 for one lane and one group: `base` is the lane's 64 bytes of the row
+// in the stage, `res_delta` the offset from there to its residual bytes.
+// With RES, z = bf16(x + r) replaces x in the stage and, when `act`, is
+// written to the residual tensor at `res_lane` (the lane's 32 values).
+template <bool RES>
+__device__ __forceinline__ void pass1_group(uint32_t base, uint32_t res_delta, int rot, bool act,
+                                            uint16_t *res_lane, float &h, float &l)
+{
+    uint32_t z[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int k = (i + rot) & 3;
+        const uint32_t a = base + uint32_t(k) * 16u;
+        uint32_t p[4];
+        lds128(a, p);
+        if (RES) {
+            uint32_t r[4];
+            lds128(a + res_delta, r);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                p[e] = pack_bf16x2(__fadd_rn(bf_lo(p[e]), bf_lo(r[e])), __fadd_rn(bf_hi(p[e]), bf_hi(r[e])));
+            if (act) {
+                sts128(a, p);
+                stg128(res_lane + k * 8, p);
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            z[4 * i + e] = p[e];
+    }
+    lane_sumsq(z, h, l);
+}
+
+// Pass 2 for one lane and one group: v = (z inv) w for the lane's 32 values
+// (z at `base` in the stage, w in weight-table line `wline`), the group scale
+// (every lane of the warp must call this: the quad shuffles name the full
+// mask) and the codes, eight per rotated piece: codes[i] belongs to piece
+// (i + rot) & 3.
+template <bool UE8M0>
+__device__ __forceinline__ float pass2_group(uint32_t base, uint32_t wline, uint32_t swz, int rot, uint64_t inv2,
+                                             uint32_t (&codes)[4][2])
+{
+    uint64_t v[4][4];
+    float mm[2] = {0.0f, 0.0f};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t k = uint32_t((i + rot) & 3);
+        uint32_t zp[4], w0[4], w1[4];
+        lds128(base + k * 16u, zp);
+        lds128(wline + ((2u * k) ^ swz) * 16u, w0);
+        lds128(wline + ((2u * k + 1u) ^ swz) * 16u, w1);
+        const uint64_t wv[4] = {(uint64_t(w0[1]) << 32) | w0[0], (uint64_t(w0[3]) << 32) | w0[2],
+                                (uint64_t(w1[1]) << 32) | w1[0], (uint64_t(w1[3]) << 32) | w1[2]};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            v[i][e] = f2_mul(f2_mul(f2_from_bf16x2(zp[e]), inv2), wv[e]);
+            float a, b;
+            f2_unpack(v[i][e], a, b);
+            mm[e & 1] = absmax3(mm[e & 1], a, b);
+        }
+    }
+    const float amax = quad_max(fmaxf(mm[0], mm[1]));
+    const float sc = group_scale<UE8M0>(amax, kScaleFloor);
+    const float rc = scale_recip<UE8M0>(sc);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        quant8<UE8M0>(v[i], sc, rc, codes[i][0], codes[i][1]);
+    return sc;
+}
+
+// -------------------------------------- warp-per-row, two passes via L2 ---
+//
+// For launches of many rows with up to 8 * kL2MaxGroups groups per row: a
+// warp owns whole rows (rows first, first + NW, ...), each lane its NG groups
+// (group 8 j + quad, j < NG).  Pass 1 reads the row from HBM straight into
+// registers, two groups ahead of the one being summed, with the default L2
+// policy so that the lines stay in L2; pass 2 reads the row again (from L2,
+// evict-first this time), one group ahead.  HBM sees each input byte once;
+// the second read costs L2 bandwidth, of which B300 has several times its
+// HBM bandwidth.  Nothing of a row is parked in shared memory (only the fp32
+// weight table is), so occupancy is set by registers alone.  With a residual,
+// pass 1 writes z = bf16(x + r) to the residual tensor and pass 2 reads z back
+// through the coherent path (each lane reads only what it wrote).
+
+constexpr int kL2MaxGroups = 8;   // per quad: 64 groups, H = 8192
+
+template <int NG, bool RES, bool V8>
+__device__ __forceinline__ void l2_load_z(const uint16_t *xr, const uint16_t *rr, int j, int quad, int sub, int G,
+                                          uint32_t (&z)[16])
+{
+    const int g = 8 * j + quad;
+    const int off = (g < G ? g : G - 1) * kGroup + sub * kValsPerLane;
+    ld64_keep<V8>(xr + off, z);
+    if (RES) {
+        uint32_t r[16];
+        ld64_rw<V8>(rr + off, r);
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+            z[e] = pack_bf16x2(__fadd_rn(bf_lo(z[e]), bf_lo(r[e])), __fadd_rn(bf_hi(z[e]), bf_hi(r[e])));
+    }
+}
+
+template <int NG, bool UE8M0, bool COL, bool RES, bool V8>
+__global__ void __launch_bounds__(kRmsMaxThreads, 2) rms_l2_kernel(
+    const uint16_t *__restrict__ x, uint16_t *__restrict__ residual, const uint16_t *__restrict__ w,
+    uint8_t *__restrict__ q, float *__restrict__ scales, int T, int H, int G, float eps)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const uint32_t wsm = smem_addr(smem);
+    const int nwarps = blockDim.x >> 5;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, sub = lane & 3, quad = lane >> 2;
+
+    wait_for_producer();
+    allow_consumer_launch();
+    fill_weight_table(w, H, wsm);
+    __syncthreads();
+
+    // the host keeps T < 2^30
+    for (int row = blockIdx.x * nwarps + warp; row < T; row += gridDim.x * nwarps) {
+        const uint16_t *xr = x + int64_t(row) * H;
+        uint16_t *rr = RES ? residual + int64_t(row) * H : nullptr;
+
+        // ---- pass 1: z into registers (two groups ahead), exact sum of squares
+        float hi = 0.0f, lo = 0.0f;
+        uint32_t buf[3][16];
+        l2_load_z<NG, RES, V8>(xr, rr, 0, quad, sub, G, buf[0]);
+        if (NG > 1)
+            l2_load_z<NG, RES, V8>(xr, rr, 1, quad, sub, G, buf[1]);
+#pragma unroll
+        for (int j = 0; j < NG; ++j) {
+            if (j + 2 < NG)
+                l2_load_z<NG, RES, V8>(xr, rr, j + 2, quad, sub, G, buf[(j + 2) % 3]);
+            const int g = 8 * j + quad;
+            const bool act = g < G;
+            if (RES && act)
+                st64<V8>(rr + g * kGroup + sub * kValsPerLane, buf[j % 3]);
+            float h, l;
+            lane_sumsq(buf[j % 3], h, l);
+            pair_add(hi, lo, act ? h : 0.0f, act ? l : 0.0f);
+        }
+#pragma unroll
+        for (int o = 1; o <= 16; o <<= 1)
+            pair_add(hi, lo, __shfl_xor_sync(0xFFFFFFFFu, hi, o), __shfl_xor_sync(0xFFFFFFFFu, lo, o));
+        const float inv = rms_inv(hi, lo, H, eps);
+        const uint64_t inv2 = f2_pack(inv, inv);
+
+        // ---- pass 2: z again (from L2, one group ahead), v = (z * inv) * w, codes
+        const uint16_t *zr = RES ? rr : xr;
+        uint32_t zb[2][16];
+        auto load2 = [&](int j, uint32_t(&dst)[16]) {
+            const int g = 8 * j + quad;
+            const int off = (g < G ? g : G - 1) * kGroup + sub * kValsPerLane;
+            if (RES)
+                ld64_rw<V8>(zr + off, dst);
+            else
+                ld64_stream<V8>(zr + off, dst);
+        };
+        load2(0, zb[0]);
+        uint8_t *q_row = q + int64_t(row) * H;
+#pragma unroll
+        for (int j = 0; j < NG; ++j) {
+            if (j + 1 < NG)
+                load2(j + 1, zb[(j + 1) & 1]);
+            const int g = 8 * j + quad;
+            const bool act = g < G;
+            const int gc = act ? g : G - 1;
+            const uint32_t line = uint32_t(gc) * 4u + uint32_t(sub);
+            const uint32_t wline = wsm + line * 128u, swz = w_swizzle(line);
+            uint64_t v[4][4];
+            float mm[2] = {0.0f, 0.0f};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t w0[4], w1[4];
+                lds128(wline + ((2u * i) ^ swz) * 16u, w0);
+                lds128(wline + ((2u * i + 1u) ^ swz) * 16u, w1);
+                const uint64_t wv[4] = {(uint64_t(w0[1]) << 32) | w0[0], (uint64_t(w0[3]) << 32) | w0[2],
+                                        (uint64_t(w1[1]) << 32) | w1[0], (uint64_t(w1[3]) << 32) | w1[2]};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    v[i][e] = f2_mul(f2_mul(f2_from_bf16x2(zb[j & 1][4 * i + e]), inv2), wv[e]);
+                    float a, b;
+                    f2_unpack(v[i][e], a, b);
+                    mm[e & 1] = absmax3(mm[e & 1], a, b);
+                }
+            }
+            const float amax = quad_max(fmaxf(mm[0], mm[1]));
+            const float sc = group_scale<UE8M0>(amax, kScaleFloor);
+            const float rc = scale_recip<UE8M0>(sc);
+            uint32_t codes[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                quant8<UE8M0>(v[i], sc, rc, codes[2 * i], codes[2 * i + 1]);
+            if (act) {
+                st32<V8>(q_row + g * kGroup + sub * kValsPerLane, codes);
+                if (sub == 0)
+                    scales[COL ? int64_t(g) * T + row : int64_t(row) * G + g] = sc;
+            }
+        }
+    }
+}
+
+// -------------------------------------------------- CTA-per-row kernel ---
+
+struct RmsCtaSmem {
+    uint32_t stage_bytes, w_off, bar_off, red_off, inv_off, total;
+
+    __host__ __device__ RmsCtaSmem(int H, bool res, int S)
     {
         stage_bytes = uint32_t(H) * 2u * (res ? 2u : 1u);
-        stages = uint32_t(S);
-        w_off = stage_bytes * stages;
-        bar_off = w_off + uint32_t(H) * 2u;                       // 256-byte aligned
-        red_off = bar_off + 8u * (kRmsMaxStages + 1);
+        w_off = stage_bytes * uint32_t(S);
+        bar_off = w_off + uint32_t(H) * 4u;
+        red_off = bar_off + 8u * kRmsMaxStages;
         inv_off = red_off + 8u * (kRmsMaxThreads / 4);
         total = inv_off + 16u;
     }
 };
 
-// Squares of one lane's 32 values (16 bf16x2 words), summed exactly:
-// returns (hi, lo) with hi + lo equal to the sum up to lo's own rounding.
-__device__ __forceinline__ void lane_sumsq(const uint32_t (&w)[16], float &hi, float &lo)
-{
-    float m = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 16; ++k)
-        m = absmax3(m, bf_lo(w[k]), bf_hi(w[k]));
-    const float pm = __fmul_rn(m, m);
-    uint64_t s = f2_pack(pm, pm), c = f2_pack(0.0f, 0.0f);
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        const uint64_t z = f2_from_bf16x2(w[k]);
-        const uint64_t p = f2_mul(z, z);
-        const uint64_t t = f2_add(s, p);
-        c = f2_add(c, f2_sub(p, f2_sub(t, s)));   // Fast2Sum error, |s| >= |p|
-        s = t;
-    }
-    float s0, s1, c0, c1;
-    f2_unpack(s, s0, s1);
-    f2_unpack(c, c0, c1);
-    const float inf = __int_as_float(0x7F800000);
-    if (!(s0 < inf && s1 < inf)) {   // the squares overflow fp32: so does the row sum
-        hi = inf;
-        lo = 0.0f;
-        return;
-    }
-    float e;
-    two_sum(__fsub_rn(s0, pm), __fsub_rn(s1, pm), hi, e);   // both differences exact
-    lo = __fadd_rn(__fadd_rn(c0, c1), e);
-}
-
 template <bool UE8M0, bool COL, bool RES>
-__global__ void __launch_bounds__(kRmsMaxThreads) rms_quant_kernel(
+__global__ void __launch_bounds__(kRmsMaxThreads) rms_cta_kernel(
     const uint16_t *__restrict__ x, uint16_t *__restrict__ residual, const uint16_t *__restrict__ w,
     uint8_t *__restrict__ q, float *__restrict__ scales, int T, int H, int G, float eps, int S)
 {
     extern __shared__ __align__(128) uint8_t smem[];
-    const RmsSmem L(H, RES, S);
+    const RmsCtaSmem L(H, RES, S);
     const uint32_t sbase = smem_addr(smem);
-    const uint32_t bar0 = sbase + L.bar_off;          // stage barriers, then the weight's
-    const uint32_t wbar = bar0 + 8u * uint32_t(S);
+    const uint32_t bar0 = sbase + L.bar_off;
+    const uint32_t wsm = sbase + L.w_off;
     float2 *red = reinterpret_cast<float2 *>(smem + L.red_off);
     float *inv_sm = reinterpret_cast<float *>(smem + L.inv_off);
 
@@ -111,73 +360,46 @@ __global__ void __launch_bounds__(kRmsMaxThreads) rms_quant_kernel(
     const uint32_t row_bytes = uint32_t(H) * 2u;
 
     if (tid == 0) {
-        for (int s = 0; s <= S; ++s)
+        for (int s = 0; s < S; ++s)
             mbar_init(bar0 + 8u * s, 1);
         fence_barrier_init();
     }
-    __syncthreads();
     wait_for_producer();
     allow_consumer_launch();
 
     const uint64_t pol_stream = policy_evict_first();
-    int issued = 0;   // row iterations whose copies thread 0 has issued
-    auto issue = [&](int j) {
+    auto issue = [&](int j) {   // thread 0: the copies of this CTA's j-th row
         const int64_t row = int64_t(blockIdx.x) + int64_t(j) * step;
-        const int s = j % S;
-        const uint32_t dst = sbase + uint32_t(s) * L.stage_bytes;
-        const uint32_t bar = bar0 + 8u * s;
+        const uint32_t dst = sbase + uint32_t(j % S) * L.stage_bytes;
+        const uint32_t bar = bar0 + 8u * uint32_t(j % S);
         mbar_arrive_expect_tx(bar, L.stage_bytes);
         bulk_g2s(dst, x + row * H, row_bytes, bar, pol_stream);
         if (RES)
             bulk_g2s(dst + row_bytes, residual + row * H, row_bytes, bar, pol_stream);
     };
-    if (tid == 0) {
-        mbar_arrive_expect_tx(wbar, row_bytes);
-        bulk_g2s(sbase + L.w_off, w, row_bytes, wbar, policy_evict_last());
+    int issued = 0;
+    if (tid == 0)
         for (; issued < S && int64_t(blockIdx.x) + int64_t(issued) * step < T; ++issued)
             issue(issued);
-    }
-    bool ok = mbar_wait(wbar, 0);
+    fill_weight_table(w, H, wsm);
+    __syncthreads();
 
     int j = 0;
     bool aborted = false;
     for (int row = blockIdx.x; row < T; row += step, ++j) {   // the host keeps T below 2^30
         const int s = j % S;
-        ok = mbar_wait(bar0 + 8u * s, uint32_t(j / S) & 1u) && ok;
+        const bool ok = mbar_wait(bar0 + 8u * s, uint32_t(j / S) & 1u);
         const uint32_t stage = sbase + uint32_t(s) * L.stage_bytes;
+        uint16_t *res_row = RES ? residual + int64_t(row) * H : nullptr;
 
-        // ---- pass 1: residual add, exact sum of squares
         float hi = 0.0f, lo = 0.0f;
         for (int gb = 0; gb < G; gb += nq) {
             const int g = gb + quad;
             const bool act = g < G;
             const int gc = act ? g : G - 1;
-            const uint32_t base = stage + uint32_t(gc) * 256u + uint32_t(sub) * 64u;
-            uint32_t z[16];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t off = uint32_t((i + rot) & 3) * 16u;
-                uint32_t p[4];
-                lds128(base + off, p);
-                if (RES) {
-                    uint32_t r[4];
-                    lds128(base + row_bytes + off, r);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        p[k] = pack_bf16x2(__fadd_rn(bf_lo(p[k]), bf_lo(r[k])),
-                                           __fadd_rn(bf_hi(p[k]), bf_hi(r[k])));
-                    if (act) {
-                        sts128(base + off, p);
-                        stg128(residual + int64_t(row) * H + gc * kGroup + sub * kValsPerLane +
-                                   ((i + rot) & 3) * 8, p);
-                    }
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    z[4 * i + k] = p[k];
-            }
             float h, l;
-            lane_sumsq(z, h, l);
+            pass1_group<RES>(stage + uint32_t(gc) * 256u + uint32_t(sub) * 64u, row_bytes, rot, act,
+                             res_row + gc * kGroup + sub * kValsPerLane, h, l);
             if (act)
                 pair_add(hi, lo, h, l);
         }
@@ -206,50 +428,30 @@ __global__ void __launch_bounds__(kRmsMaxThreads) rms_quant_kernel(
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1)
                 pair_add(a.x, a.y, __shfl_xor_sync(0xFFFFFFFFu, a.x, o), __shfl_xor_sync(0xFFFFFFFFu, a.y, o));
-            if (lane == 0) {
-                const float ss = __fadd_rn(a.x, a.y);
-                inv_sm[0] = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(ss, float(H)), eps)));
-            }
+            if (lane == 0)
+                inv_sm[0] = rms_inv(a.x, a.y, H, eps);
         }
         __syncthreads();
         const float inv = inv_sm[0];
         const uint64_t inv2 = f2_pack(inv, inv);
 
-        // ---- pass 2: v = (z * inv) * w, group scale, codes
+        uint8_t *q_row = q + int64_t(row) * H;
         for (int gb = 0; gb < G; gb += nq) {
             const int g = gb + quad;
             const bool act = g < G;
             const int gc = act ? g : G - 1;
-            const uint32_t off_g = uint32_t(gc) * 256u + uint32_t(sub) * 64u;
-            uint64_t v[4][4];
-            float m = 0.0f;
+            const uint32_t line = uint32_t(gc) * 4u + uint32_t(sub);
+            uint32_t codes[4][2];
+            const float sc = pass2_group<UE8M0>(stage + uint32_t(gc) * 256u + uint32_t(sub) * 64u,
+                                                wsm + line * 128u, w_swizzle(line), rot, inv2, codes);
+            if (act) {
+                uint8_t *ql = q_row + gc * kGroup + sub * kValsPerLane;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t off = off_g + uint32_t((i + rot) & 3) * 16u;
-                uint32_t zp[4], wp[4];
-                lds128(stage + off, zp);
-                lds128(sbase + L.w_off + off, wp);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    v[i][k] = f2_mul(f2_mul(f2_from_bf16x2(zp[k]), inv2), f2_from_bf16x2(wp[k]));
-                    float a, b;
-                    f2_unpack(v[i][k], a, b);
-                    m = absmax3(m, a, b);
-                }
+                for (int i = 0; i < 4; ++i)
+                    stg64(ql + ((i + rot) & 3) * 8, codes[i][0], codes[i][1]);
+                if (sub == 0)
+                    scales[COL ? int64_t(g) * T + row : int64_t(row) * G + g] = sc;
             }
-            const float amax = quad_max(m);
-            const float sc = group_scale<UE8M0>(amax, kScaleFloor);
-            const float rc = scale_recip<UE8M0>(sc);
-            uint8_t *qrow = q + int64_t(row) * H + gc * kGroup + sub * kValsPerLane;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                uint32_t c0, c1;
-                quant8<UE8M0>(v[i], sc, rc, c0, c1);
-                if (act)
-                    stg64(qrow + ((i + rot) & 3) * 8, c0, c1);
-            }
-            if (act && sub == 0)
-                scales[COL ? int64_t(g) * T + row : int64_t(row) * G + g] = sc;
         }
         if (RES)
             fence_proxy_async();   // z was written to the stage the copy engine refills next
@@ -266,9 +468,7 @@ __global__ void __launch_bounds__(kRmsMaxThreads) rms_quant_kernel(
 
     if (aborted && tid == 0) {
         raise_device_error(kErrBarrierTimeout);
-        // let the copies still in flight land before shared memory goes away
-        mbar_wait(wbar, 0);
-        for (int k = j; k < issued; ++k)
+        for (int k = j; k < issued; ++k)   // let copies in flight land first
             mbar_wait(bar0 + 8u * (k % S), uint32_t(k / S) & 1u);
     }
 }

@@ -67,8 +67,10 @@ typedef enum {
     FP8Q_SCALES_COL_MAJOR = 1  /* s[g*T + t] */
 } fp8q_scale_layout;
 
-/* Longest rms_norm_per_block_quant row (H) the kernels accept. */
+/* Longest rms_norm_per_block_quant row (H) the kernels accept: a row, its
+ * residual row and the weight (as fp32) are held in shared memory. */
 #define FP8Q_RMS_MAX_H 32768
+#define FP8Q_RMS_MAX_H_RESIDUAL 16384
 
 /*
  * per_token_group_fp8_quant.
@@ -102,7 +104,8 @@ FP8Q_API int fp8q_per_token_group_quant(const void *x, void *q, float *scales, i
  * RN32(RN32(ss/H) + eps)))); v_h = RN32(RN32(z_h * inv) * w_h); then the
  * group quantisation of v.  Outside the underflow case the result is
  * therefore the same, bit for bit, as a sequential evaluation of these steps
- * with the sum carried in double precision.  H <= FP8Q_RMS_MAX_H,
+ * with the sum carried in double precision.  H <= FP8Q_RMS_MAX_H
+ * (FP8Q_RMS_MAX_H_RESIDUAL with a residual), else FP8Q_ERR_UNSUPPORTED;
  * T < 2^30.  Rows are staged in shared memory by bulk asynchronous copies;
  * a kernel that waited more than about a second for one gives up, leaves the
  * remaining rows unwritten and sets FP8Q_DEVICE_ERR_TIMEOUT (see

@@ -190,6 +190,8 @@ def test_rms_qwen3_mix(T):
                                  (3, 24576), (2, 32768), (300, 256), (700, 8192), (1, 8320)])
 @pytest.mark.parametrize("residual", [False, True], ids=["plain", "residual"])
 def test_rms_ragged_shapes(T, H, residual):
+    if residual and H > 16384:
+        pytest.skip("rows with a residual are limited to 16384 values (FP8Q_ERR_UNSUPPORTED, tested on CPU)")
     x, w, r = inputs.rms_input(T, H, seeds=(900 + T, 901 + H, 902))
     for ue8m0, col in VARIANTS:
         _check_rms(inputs.bits(x), inputs.bits(w), inputs.bits(r) if residual else None, ue8m0, col,
@@ -311,3 +313,17 @@ def test_no_device_error_raised():
     gpu_silu(inputs.bits(inputs.silu_input(8, 1024)), True, False)
     gpu_group_quant(inputs.bits(inputs.small_group_quant_input()))
     assert fq.fp8q_take_device_error() == 0
+
+
+@pytest.mark.parametrize("T,H,residual", [(1100, 4096, True), (1024, 5120, False), (2048, 8192, True),
+                                          (1500, 384, True), (1031, 1152, False)])
+def test_rms_many_rows_bit_exact(T, H, residual):
+    """Launches of 1024 rows or more take the warp-per-row kernel."""
+    x, w, r = inputs.rms_input(T, H, seeds=(910 + T, 911 + H, 912))
+    xb, wb, rb = inputs.bits(x), inputs.bits(w), inputs.bits(r) if residual else None
+    for ue8m0, col in VARIANTS:
+        q, s, rout = gpu_rms(xb, wb, rb, ue8m0, col)
+        qr, sr, _, _, ror = oracle.rms_norm_per_block_quant(xb, wb, rb, ue8m0=ue8m0, col_major=col)
+        assert_exact(q, s, qr, to_tg(sr, col), f"rms T={T} H={H} residual={residual}")
+        if residual:
+            assert np.array_equal(rout, ror)
