@@ -376,8 +376,11 @@ class DeviceStep:
 
 
 def time_device(step: DeviceStep, steps: int, warmup: int, dist: Dist):
-    """K steps of the three launches, bracketed by barrier + synchronize.
-    Events around every launch give each kernel's average duration."""
+    """K steps of the three launches back to back, bracketed by barrier +
+    synchronize, timed with one pair of CUDA events on the launching stream
+    (an event between two kernels would stop the second from being
+    scheduled while the first drains).  Then K more steps with an event
+    after every launch give each kernel's average duration."""
     import torch
 
     st = step.stream
@@ -385,23 +388,28 @@ def time_device(step: DeviceStep, steps: int, warmup: int, dist: Dist):
         for op in step.ops:
             step.launch(op)
     torch.cuda.synchronize()
-    per_op = {op: [] for op in step.ops}
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(step.ops) + 1)] for _ in range(steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     dist.barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     start.record(st)
-    for k in range(steps):
-        ev[k][0].record(st)
-        for i, op in enumerate(step.ops):
+    for _ in range(steps):
+        for op in step.ops:
             step.launch(op)
-            ev[k][i + 1].record(st)
     end.record(st)
     torch.cuda.synchronize()
     t1 = time.perf_counter()
     dist.barrier()
     total_ms = start.elapsed_time(end)
+
+    per_op = {op: [] for op in step.ops}
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(step.ops) + 1)] for _ in range(steps)]
+    for k in range(steps):
+        ev[k][0].record(st)
+        for i, op in enumerate(step.ops):
+            step.launch(op)
+            ev[k][i + 1].record(st)
+    torch.cuda.synchronize()
     for k in range(steps):
         for i, op in enumerate(step.ops):
             per_op[op].append(ev[k][i].elapsed_time(ev[k][i + 1]))

@@ -163,16 +163,20 @@ cudaError_t launch_silu(const uint16_t *x, uint8_t *q, float *s, int64_t n, int6
                   dim3{unsigned(kCtaThreads)}, st, x, q, s, n, G, T, I, eps);
 }
 
-// rms_norm_per_block_quant, one CTA per row: as many row stages (up to 8) as
-// fit three CTAs per SM, else two, else one CTA with whatever fits.
+// rms_norm_per_block_quant, one CTA per row: at least three row stages with
+// four CTAs per SM if they fit, else at least two with three or two CTAs per
+// SM, else one CTA with whatever fits; within a budget, as many stages (up to
+// 8) as fit.
 int rms_cta_stages(int H, bool res)
 {
-    for (uint32_t budget : {72u * 1024u, 110u * 1024u, kSmemPerCtaMax}) {
-        for (int S = kRmsMaxStages; S >= 1; --S) {
-            if (RmsCtaSmem(H, res, S).total <= budget && (S >= 2 || budget == kSmemPerCtaMax))
+    const struct {
+        uint32_t budget;
+        int min_stages;
+    } tiers[] = {{55u * 1024u, 3}, {72u * 1024u, 2}, {110u * 1024u, 2}, {kSmemPerCtaMax, 1}};
+    for (const auto &t : tiers)
+        for (int S = kRmsMaxStages; S >= t.min_stages; --S)
+            if (RmsCtaSmem(H, res, S).total <= t.budget)
                 return S;
-        }
-    }
     return 0;
 }
 
@@ -209,34 +213,58 @@ cudaError_t launch_rms_cta(const uint16_t *x, uint16_t *res, const uint16_t *w, 
                        T, H, G, eps, S);
 }
 
-// rms_norm_per_block_quant, one warp per row, two passes (the second from
-// L2): resident CTAs of 8 warps, no more than there are rows for.
-template <int NG, bool U, bool C, bool R, bool V>
-cudaError_t launch_rms_l2(const uint16_t *x, uint16_t *res, const uint16_t *w, uint8_t *q, float *s, int T,
-                          int H, int G, float eps, cudaStream_t st)
+// rms_norm_per_block_quant, one warp per row: the warps per CTA that give the
+// most resident warps per SM (each warp holds one row stage).
+struct WarpShape {
+    int warps = 0, per_sm = 0;
+};
+
+template <typename K>
+WarpShape rms_warp_shape(K kernel, int H, bool res)
 {
-    auto kernel = rms_l2_kernel<NG, U, C, R, V>;
-    constexpr int kWarps = kRmsMaxThreads / 32;
-    const uint32_t smem = uint32_t(H) * 4u;   // the fp32 weight table
-    const int dev = current_device();
-    int per_sm = 0, unused_a = 0, unused_b = 0;
-    if (!shape_cache().find(dev, reinterpret_cast<const void *>(kernel), H, per_sm, unused_a, unused_b)) {
-        cudaError_t e = allow_smem(kernel, kSmemPerCtaMax);
-        if (e != cudaSuccess)
-            return e;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kRmsMaxThreads, smem) != cudaSuccess ||
-            per_sm < 1) {
-            cudaGetLastError();
-            per_sm = 1;
-        }
-        shape_cache().put(dev, reinterpret_cast<const void *>(kernel), H, per_sm, 0, 0);
+    WarpShape best;
+    if (allow_smem(kernel, kSmemPerCtaMax) != cudaSuccess) {
+        cudaGetLastError();
+        return best;
     }
-    int64_t grid = int64_t(per_sm) * sm_count();
-    const int64_t need = (T + kWarps - 1) / kWarps;
+    for (int W : {8, 6, 4, 2}) {
+        const uint32_t smem = RmsWarpSmem(H, res, W).total;
+        if (smem > kSmemPerCtaMax)
+            continue;
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 32 * W, smem) != cudaSuccess)
+            continue;
+        if (per_sm * W > best.per_sm * best.warps) {
+            best.warps = W;
+            best.per_sm = per_sm;
+        }
+    }
+    cudaGetLastError();
+    return best;
+}
+
+template <bool U, bool C, bool R>
+cudaError_t launch_rms_warp(const uint16_t *x, uint16_t *res, const uint16_t *w, uint8_t *q, float *s, int T,
+                            int H, int G, float eps, cudaStream_t st, bool &launched)
+{
+    auto kernel = rms_warp_kernel<U, C, R>;
+    const int dev = current_device();
+    WarpShape ws;
+    int unused = 0;
+    if (!shape_cache().find(dev, reinterpret_cast<const void *>(kernel), H, ws.warps, ws.per_sm, unused)) {
+        ws = rms_warp_shape(kernel, H, R);
+        shape_cache().put(dev, reinterpret_cast<const void *>(kernel), H, ws.warps, ws.per_sm, 0);
+    }
+    launched = ws.warps > 0 && ws.warps * ws.per_sm >= 4;
+    if (!launched)
+        return cudaSuccess;
+    int64_t grid = int64_t(ws.per_sm) * sm_count();
+    const int64_t need = (T + ws.warps - 1) / ws.warps;
     if (need < grid)
         grid = need;
-    return launch_smem(kernel, dim3{unsigned(grid)}, dim3{unsigned(kRmsMaxThreads)}, smem, st, x, res, w, q, s, T,
-                       H, G, eps);
+    const uint32_t smem = RmsWarpSmem(H, R, ws.warps).total;
+    return launch_smem(kernel, dim3{unsigned(grid)}, dim3{unsigned(32 * ws.warps)}, smem, st, x, res, w, q, s, T, H,
+                       G, eps);
 }
 
 // Rows per launch from which the warp-per-row kernel takes over: below it a
@@ -244,21 +272,15 @@ cudaError_t launch_rms_l2(const uint16_t *x, uint16_t *res, const uint16_t *w, u
 // 64 quads.
 constexpr int kRmsWarpMinRows = 1024;
 
-template <bool U, bool C, bool R, bool V>
+template <bool U, bool C, bool R>
 cudaError_t launch_rms(const uint16_t *x, uint16_t *res, const uint16_t *w, uint8_t *q, float *s,
                        int T, int H, int G, float eps, cudaStream_t st)
 {
-    if (T >= kRmsWarpMinRows && G <= 8 * kL2MaxGroups) {
-        switch ((G + 7) / 8) {
-        case 1: return launch_rms_l2<1, U, C, R, V>(x, res, w, q, s, T, H, G, eps, st);
-        case 2: return launch_rms_l2<2, U, C, R, V>(x, res, w, q, s, T, H, G, eps, st);
-        case 3: return launch_rms_l2<3, U, C, R, V>(x, res, w, q, s, T, H, G, eps, st);
-        case 4: return launch_rms_l2<4, U, C, R, V>(x, res, w, q, s, T, H, G, eps, st);
-        case 5: return launch_rms_l2<5, U, C, R, V>(x, res, w, q, s, T, H, G, eps, st);
-        case 6: return launch_rms_l2<6, U, C, R, V>(x, res, w, q, s, T, H, G, eps, st);
-        case 7: return launch_rms_l2<7, U, C, R, V>(x, res, w, q, s, T, H, G, eps, st);
-        default: return launch_rms_l2<8, U, C, R, V>(x, res, w, q, s, T, H, G, eps, st);
-        }
+    if (T >= kRmsWarpMinRows && G <= 8 * kWarpMaxSegs) {
+        bool launched = false;
+        const cudaError_t e = launch_rms_warp<U, C, R>(x, res, w, q, s, T, H, G, eps, st, launched);
+        if (launched || e != cudaSuccess)
+            return e;
     }
     return launch_rms_cta<U, C, R>(x, res, w, q, s, T, H, G, eps, st);
 }
@@ -359,17 +381,14 @@ int fp8q_rms_norm_per_block_quant(const void *x, void *residual, const void *wei
     const bool col = scale_layout == FP8Q_SCALES_COL_MAJOR;
     const int t = int(T), h = int(H);
     cudaError_t e;
-    const bool v8 = aligned(x, 32) && aligned(q, 32) && (!rp || aligned(rp, 32));
-#define FP8Q_RMS_V(U, C, R)                                                                      \
-    (v8 ? launch_rms<U, C, R, true>(xp, rp, wp, qp, scales, t, h, G, eps, st)                   \
-        : launch_rms<U, C, R, false>(xp, rp, wp, qp, scales, t, h, G, eps, st))
-#define FP8Q_RMS(U, C) (rp ? FP8Q_RMS_V(U, C, true) : FP8Q_RMS_V(U, C, false))
+#define FP8Q_RMS(U, C)                                                                           \
+    (rp ? launch_rms<U, C, true>(xp, rp, wp, qp, scales, t, h, G, eps, st)                      \
+        : launch_rms<U, C, false>(xp, rp, wp, qp, scales, t, h, G, eps, st))
     if (ue8m0)
         e = col ? FP8Q_RMS(true, true) : FP8Q_RMS(true, false);
     else
         e = col ? FP8Q_RMS(false, true) : FP8Q_RMS(false, false);
 #undef FP8Q_RMS
-#undef FP8Q_RMS_V
     return launch_status(e);
 }
 

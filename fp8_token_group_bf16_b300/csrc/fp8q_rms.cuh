@@ -4,9 +4,9 @@
 //
 // Two kernels share the per-row arithmetic below:
 //
-//  * rms_l2_kernel (many rows of up to 8192 values): a warp owns whole rows
-//    and reads each row twice, from HBM into registers for the sum of
-//    squares and from L2 for the quantisation (details at the kernel).
+//  * rms_warp_kernel (many rows of up to 8192 values): a warp owns whole
+//    rows; one row stage per warp, refilled segment by segment with the next
+//    row while the warp quantises the current one (details at the kernel).
 //  * rms_cta_kernel (few rows, decode sizes, and longer rows): a CTA of one
 //    quad per group owns a row, so a row's work is spread over up to 64
 //    quads; the row is staged in shared memory by bulk asynchronous copies
@@ -193,75 +193,102 @@ __device__ __forceinline__ float pass2_group(uint32_t base, uint32_t wline, uint
     return sc;
 }
 
-// -------------------------------------- warp-per-row, two passes via L2 ---
+// ----------------------------------------- warp-per-row, rolling stage ---
 //
-// For launches of many rows with up to 8 * kL2MaxGroups groups per row: a
-// warp owns whole rows (rows first, first + NW, ...), each lane its NG groups
-// (group 8 j + quad, j < NG).  Pass 1 reads the row from HBM straight into
-// registers, two groups ahead of the one being summed, with the default L2
-// policy so that the lines stay in L2; pass 2 reads the row again (from L2,
-// evict-first this time), one group ahead.  HBM sees each input byte once;
-// the second read costs L2 bandwidth, of which B300 has several times its
-// HBM bandwidth.  Nothing of a row is parked in shared memory (only the fp32
-// weight table is), so occupancy is set by registers alone.  With a residual,
-// pass 1 writes z = bf16(x + r) to the residual tensor and pass 2 reads z back
-// through the coherent path (each lane reads only what it wrote).
+// For launches of many rows with up to 8 * kWarpMaxSegs groups per row: a
+// warp owns whole rows (rows first, first + NW, ...), each lane its groups
+// 8 j + quad.  The warp has one row stage in shared memory, cut into
+// segments of 8 groups (2 KiB of bf16), each with its own mbarrier.  Pass 1
+// waits for the segments in order; pass 2 reads them again and, as soon as
+// the warp is done with segment j, lane 0 starts the copy of segment j of the
+// warp's next row into it.  The next row therefore streams in while pass 2
+// runs, with one stage per warp instead of two, which doubles the warps a
+// SM can hold (shared memory, not registers, bounds them otherwise).
 
-constexpr int kL2MaxGroups = 8;   // per quad: 64 groups, H = 8192
+constexpr int kWarpMaxSegs = 8;           // rows of up to 64 groups (8192 values)
+constexpr uint32_t kSegBytes = 8u * 256u;  // 8 groups of bf16
 
-template <int NG, bool RES, bool V8>
-__device__ __forceinline__ void l2_load_z(const uint16_t *xr, const uint16_t *rr, int j, int quad, int sub, int G,
-                                          uint32_t (&z)[16])
-{
-    const int g = 8 * j + quad;
-    const int off = (g < G ? g : G - 1) * kGroup + sub * kValsPerLane;
-    ld64_keep<V8>(xr + off, z);
-    if (RES) {
-        uint32_t r[16];
-        ld64_rw<V8>(rr + off, r);
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-            z[e] = pack_bf16x2(__fadd_rn(bf_lo(z[e]), bf_lo(r[e])), __fadd_rn(bf_hi(z[e]), bf_hi(r[e])));
+struct RmsWarpSmem {
+    uint32_t stage_bytes, w_off, bar_off, total;
+
+    __host__ __device__ RmsWarpSmem(int H, bool res, int warps)
+    {
+        stage_bytes = uint32_t(H) * 2u * (res ? 2u : 1u);
+        w_off = stage_bytes * uint32_t(warps);
+        bar_off = w_off + uint32_t(H) * 4u;
+        total = bar_off + 8u * kWarpMaxSegs * uint32_t(warps);
     }
-}
+};
 
-template <int NG, bool UE8M0, bool COL, bool RES, bool V8>
-__global__ void __launch_bounds__(kRmsMaxThreads, 2) rms_l2_kernel(
+template <bool UE8M0, bool COL, bool RES>
+__global__ void __launch_bounds__(kRmsMaxThreads, 2) rms_warp_kernel(
     const uint16_t *__restrict__ x, uint16_t *__restrict__ residual, const uint16_t *__restrict__ w,
     uint8_t *__restrict__ q, float *__restrict__ scales, int T, int H, int G, float eps)
 {
     extern __shared__ __align__(128) uint8_t smem[];
-    const uint32_t wsm = smem_addr(smem);
     const int nwarps = blockDim.x >> 5;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, sub = lane & 3, quad = lane >> 2;
+    const RmsWarpSmem L(H, RES, nwarps);
+    const uint32_t sbase = smem_addr(smem);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, sub = lane & 3, quad = lane >> 2;
+    const int rot = (lane >> 1) & 3;
+    const uint32_t row_bytes = uint32_t(H) * 2u;
+    const uint32_t stage = sbase + uint32_t(warp) * L.stage_bytes;   // this warp's
+    const uint32_t bars = sbase + L.bar_off + 8u * kWarpMaxSegs * uint32_t(warp);
+    const uint32_t wsm = sbase + L.w_off;
+    const int nseg = (G + 7) / 8;   // <= kWarpMaxSegs (host)
 
+    if (lane == 0) {
+        for (int j = 0; j < nseg; ++j)
+            mbar_init(bars + 8u * j, 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
     wait_for_producer();
     allow_consumer_launch();
+
+    // rows of this warp: first, first + rstep, ...  (the host keeps T < 2^30)
+    const int first = blockIdx.x * nwarps + warp;
+    const int rstep = gridDim.x * nwarps;
+    auto issue_seg = [&](int64_t row, int j) {   // lane 0
+        const uint32_t off = kSegBytes * uint32_t(j);
+        const uint32_t n = row_bytes - off < kSegBytes ? row_bytes - off : kSegBytes;
+        const uint32_t bar = bars + 8u * uint32_t(j);
+        const uint64_t pol = policy_evict_first();
+        mbar_arrive_expect_tx(bar, RES ? 2u * n : n);
+        bulk_g2s(stage + off, reinterpret_cast<const char *>(x + row * H) + off, n, bar, pol);
+        if (RES)
+            bulk_g2s(stage + row_bytes + off, reinterpret_cast<const char *>(residual + row * H) + off, n, bar,
+                     pol);
+    };
+    if (lane == 0 && first < T)
+        for (int j = 0; j < nseg; ++j)
+            issue_seg(first, j);
     fill_weight_table(w, H, wsm);
     __syncthreads();
 
-    // the host keeps T < 2^30
-    for (int row = blockIdx.x * nwarps + warp; row < T; row += gridDim.x * nwarps) {
-        const uint16_t *xr = x + int64_t(row) * H;
-        uint16_t *rr = RES ? residual + int64_t(row) * H : nullptr;
+    int k = 0;
+    bool aborted = false;
+    for (int row = first; row < T; row += rstep, ++k) {
+        const uint32_t par = uint32_t(k) & 1u;
+        const int64_t next = int64_t(row) + rstep;
+        uint16_t *res_row = RES ? residual + int64_t(row) * H : nullptr;
 
-        // ---- pass 1: z into registers (two groups ahead), exact sum of squares
+        // ---- pass 1: residual add, exact sum of squares, segment by segment
+        bool ok = true;
         float hi = 0.0f, lo = 0.0f;
-        uint32_t buf[3][16];
-        l2_load_z<NG, RES, V8>(xr, rr, 0, quad, sub, G, buf[0]);
-        if (NG > 1)
-            l2_load_z<NG, RES, V8>(xr, rr, 1, quad, sub, G, buf[1]);
-#pragma unroll
-        for (int j = 0; j < NG; ++j) {
-            if (j + 2 < NG)
-                l2_load_z<NG, RES, V8>(xr, rr, j + 2, quad, sub, G, buf[(j + 2) % 3]);
+        for (int j = 0; j < nseg; ++j) {
+            ok = mbar_wait(bars + 8u * j, par) && ok;
             const int g = 8 * j + quad;
             const bool act = g < G;
-            if (RES && act)
-                st64<V8>(rr + g * kGroup + sub * kValsPerLane, buf[j % 3]);
+            const int gc = act ? g : G - 1;
             float h, l;
-            lane_sumsq(buf[j % 3], h, l);
+            pass1_group<RES>(stage + uint32_t(gc) * 256u + uint32_t(sub) * 64u, row_bytes, rot, act,
+                             res_row + gc * kGroup + sub * kValsPerLane, h, l);
             pair_add(hi, lo, act ? h : 0.0f, act ? l : 0.0f);
+        }
+        if (__any_sync(0xFFFFFFFFu, !ok)) {
+            aborted = true;
+            break;
         }
 #pragma unroll
         for (int o = 1; o <= 16; o <<= 1)
@@ -269,65 +296,44 @@ __global__ void __launch_bounds__(kRmsMaxThreads, 2) rms_l2_kernel(
         const float inv = rms_inv(hi, lo, H, eps);
         const uint64_t inv2 = f2_pack(inv, inv);
 
-        // ---- pass 2: z again (from L2, one group ahead), v = (z * inv) * w, codes
-        const uint16_t *zr = RES ? rr : xr;
-        uint32_t zb[2][16];
-        auto load2 = [&](int j, uint32_t(&dst)[16]) {
-            const int g = 8 * j + quad;
-            const int off = (g < G ? g : G - 1) * kGroup + sub * kValsPerLane;
-            if (RES)
-                ld64_rw<V8>(zr + off, dst);
-            else
-                ld64_stream<V8>(zr + off, dst);
-        };
-        load2(0, zb[0]);
+        // ---- pass 2: v = (z * inv) * w, codes; each segment refilled once read
         uint8_t *q_row = q + int64_t(row) * H;
-#pragma unroll
-        for (int j = 0; j < NG; ++j) {
-            if (j + 1 < NG)
-                load2(j + 1, zb[(j + 1) & 1]);
+        for (int j = 0; j < nseg; ++j) {
             const int g = 8 * j + quad;
             const bool act = g < G;
             const int gc = act ? g : G - 1;
             const uint32_t line = uint32_t(gc) * 4u + uint32_t(sub);
-            const uint32_t wline = wsm + line * 128u, swz = w_swizzle(line);
-            uint64_t v[4][4];
-            float mm[2] = {0.0f, 0.0f};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                uint32_t w0[4], w1[4];
-                lds128(wline + ((2u * i) ^ swz) * 16u, w0);
-                lds128(wline + ((2u * i + 1u) ^ swz) * 16u, w1);
-                const uint64_t wv[4] = {(uint64_t(w0[1]) << 32) | w0[0], (uint64_t(w0[3]) << 32) | w0[2],
-                                        (uint64_t(w1[1]) << 32) | w1[0], (uint64_t(w1[3]) << 32) | w1[2]};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    v[i][e] = f2_mul(f2_mul(f2_from_bf16x2(zb[j & 1][4 * i + e]), inv2), wv[e]);
-                    float a, b;
-                    f2_unpack(v[i][e], a, b);
-                    mm[e & 1] = absmax3(mm[e & 1], a, b);
-                }
+            uint32_t codes[4][2];
+            const float sc = pass2_group<UE8M0>(stage + uint32_t(gc) * 256u + uint32_t(sub) * 64u,
+                                                wsm + line * 128u, w_swizzle(line), rot, inv2, codes);
+            if (RES)
+                fence_proxy_async();   // z was written to this segment in pass 1
+            __syncwarp();
+            if (lane == 0 && next < T) {
+                fence_proxy_async();
+                issue_seg(next, j);
             }
-            const float amax = quad_max(fmaxf(mm[0], mm[1]));
-            const float sc = group_scale<UE8M0>(amax, kScaleFloor);
-            const float rc = scale_recip<UE8M0>(sc);
-            uint32_t codes[8];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                quant8<UE8M0>(v[i], sc, rc, codes[2 * i], codes[2 * i + 1]);
             if (act) {
-                st32<V8>(q_row + g * kGroup + sub * kValsPerLane, codes);
+                uint8_t *ql = q_row + gc * kGroup + sub * kValsPerLane;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    stg64(ql + ((i + rot) & 3) * 8, codes[i][0], codes[i][1]);
                 if (sub == 0)
                     scales[COL ? int64_t(g) * T + row : int64_t(row) * G + g] = sc;
             }
         }
+    }
+    if (aborted && lane == 0) {
+        raise_device_error(kErrBarrierTimeout);
+        for (int j = 0; j < nseg; ++j)   // the current row's copies: let them land first
+            mbar_wait(bars + 8u * j, uint32_t(k) & 1u);
     }
 }
 
 // -------------------------------------------------- CTA-per-row kernel ---
 
 struct RmsCtaSmem {
-    uint32_t stage_bytes, w_off, bar_off, red_off, inv_off, total;
+    uint32_t stage_bytes, w_off, bar_off, red_off, total;
 
     __host__ __device__ RmsCtaSmem(int H, bool res, int S)
     {
@@ -335,13 +341,12 @@ struct RmsCtaSmem {
         w_off = stage_bytes * uint32_t(S);
         bar_off = w_off + uint32_t(H) * 4u;
         red_off = bar_off + 8u * kRmsMaxStages;
-        inv_off = red_off + 8u * (kRmsMaxThreads / 4);
-        total = inv_off + 16u;
+        total = red_off + 2u * 8u * (kRmsMaxThreads / 32);   // a (hi, lo) pair per warp, double-buffered
     }
 };
 
 template <bool UE8M0, bool COL, bool RES>
-__global__ void __launch_bounds__(kRmsMaxThreads) rms_cta_kernel(
+__global__ void __launch_bounds__(kRmsMaxThreads, 3) rms_cta_kernel(
     const uint16_t *__restrict__ x, uint16_t *__restrict__ residual, const uint16_t *__restrict__ w,
     uint8_t *__restrict__ q, float *__restrict__ scales, int T, int H, int G, float eps, int S)
 {
@@ -351,10 +356,9 @@ __global__ void __launch_bounds__(kRmsMaxThreads) rms_cta_kernel(
     const uint32_t bar0 = sbase + L.bar_off;
     const uint32_t wsm = sbase + L.w_off;
     float2 *red = reinterpret_cast<float2 *>(smem + L.red_off);
-    float *inv_sm = reinterpret_cast<float *>(smem + L.inv_off);
 
     const int tid = threadIdx.x, lane = tid & 31, sub = tid & 3, quad = tid >> 2;
-    const int nq = blockDim.x >> 2;
+    const int nq = blockDim.x >> 2, nwarps = blockDim.x >> 5;
     const int rot = (lane >> 1) & 3;
     const int step = gridDim.x;
     const uint32_t row_bytes = uint32_t(H) * 2u;
@@ -403,11 +407,15 @@ __global__ void __launch_bounds__(kRmsMaxThreads) rms_cta_kernel(
             if (act)
                 pair_add(hi, lo, h, l);
         }
+        // each warp adds its lanes' partial sums, exactly; one (hi, lo) per warp
+        // goes to shared memory (two buffers, alternating by row, so that a
+        // warp may write the next row's pair while a slower one still reads)
 #pragma unroll
-        for (int o = 1; o <= 2; o <<= 1)
+        for (int o = 1; o <= 16; o <<= 1)
             pair_add(hi, lo, __shfl_xor_sync(0xFFFFFFFFu, hi, o), __shfl_xor_sync(0xFFFFFFFFu, lo, o));
-        if (sub == 0)
-            red[quad] = make_float2(hi, lo);
+        float2 *red_row = red + (j & 1) * (kRmsMaxThreads / 32);
+        if (lane == 0)
+            red_row[tid >> 5] = make_float2(hi, lo);
 
         if (__syncthreads_or(!ok)) {
             aborted = true;
@@ -419,20 +427,13 @@ __global__ void __launch_bounds__(kRmsMaxThreads) rms_cta_kernel(
             issue(j - 1 + S);
             issued = j + S;
         }
-        if (tid < 32) {
-            float2 a = lane < nq ? red[lane] : make_float2(0.0f, 0.0f);
-            if (lane + 32 < nq) {
-                const float2 b = red[lane + 32];
-                pair_add(a.x, a.y, b.x, b.y);
-            }
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1)
-                pair_add(a.x, a.y, __shfl_xor_sync(0xFFFFFFFFu, a.x, o), __shfl_xor_sync(0xFFFFFFFFu, a.y, o));
-            if (lane == 0)
-                inv_sm[0] = rms_inv(a.x, a.y, H, eps);
+        // every thread adds the warps' pairs in the same order
+        float2 a = red_row[0];
+        for (int i = 1; i < nwarps; ++i) {
+            const float2 b = red_row[i];
+            pair_add(a.x, a.y, b.x, b.y);
         }
-        __syncthreads();
-        const float inv = inv_sm[0];
+        const float inv = rms_inv(a.x, a.y, H, eps);
         const uint64_t inv2 = f2_pack(inv, inv);
 
         uint8_t *q_row = q + int64_t(row) * H;
