@@ -276,7 +276,7 @@ template <bool U, bool C, bool R>
 cudaError_t launch_rms(const uint16_t *x, uint16_t *res, const uint16_t *w, uint8_t *q, float *s,
                        int T, int H, int G, float eps, cudaStream_t st)
 {
-    if (T >= kRmsWarpMinRows && G <= 8 * kWarpMaxSegs) {
+    if (T >= kRmsWarpMinRows && G <= kSegGroups * kWarpMaxSegs) {
         bool launched = false;
         const cudaError_t e = launch_rms_warp<U, C, R>(x, res, w, q, s, T, H, G, eps, st, launched);
         if (launched || e != cudaSuccess)

@@ -128,7 +128,7 @@ __device__ __forceinline__ uint64_t silu_mul2(uint32_t aw, uint32_t bw)
 }
 
 template <bool UE8M0, bool COL, bool V8>
-__global__ void __launch_bounds__(kCtaThreads, 3) silu_quant_kernel(const uint16_t *__restrict__ x,
+__global__ void __launch_bounds__(kCtaThreads, 4) silu_quant_kernel(const uint16_t *__restrict__ x,
                                                                  uint8_t *__restrict__ q,
                                                                  float *__restrict__ scales,
                                                                  int64_t n_groups, int64_t G,
