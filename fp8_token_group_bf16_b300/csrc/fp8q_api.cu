@@ -272,17 +272,32 @@ cudaError_t launch_rms_warp(const uint16_t *x, uint16_t *res, const uint16_t *w,
 // 64 quads.
 constexpr int kRmsWarpMinRows = 1024;
 
+// rms_norm_per_block_quant, one CTA per row with the row in registers: one
+// quad per group up to 64 groups, 2 or 4 groups per quad beyond.
+template <int NG, bool U, bool C, bool R, bool V>
+cudaError_t launch_rms_row(const uint16_t *x, uint16_t *res, const uint16_t *w, uint8_t *q, float *s, int T,
+                           int H, int G, float eps, cudaStream_t st)
+{
+    const int quads = (G + NG - 1) / NG;
+    const int threads = ((quads * 4 + 31) / 32) * 32;
+    return launch(rms_row_kernel<NG, U, C, R, V>, dim3{unsigned(T)}, dim3{unsigned(threads)}, st, x, res, w, q, s,
+                  T, H, G, eps);
+}
+
 template <bool U, bool C, bool R>
 cudaError_t launch_rms(const uint16_t *x, uint16_t *res, const uint16_t *w, uint8_t *q, float *s,
                        int T, int H, int G, float eps, cudaStream_t st)
 {
-    if (T >= kRmsWarpMinRows && G <= kSegGroups * kWarpMaxSegs) {
-        bool launched = false;
-        const cudaError_t e = launch_rms_warp<U, C, R>(x, res, w, q, s, T, H, G, eps, st, launched);
-        if (launched || e != cudaSuccess)
-            return e;
-    }
-    return launch_rms_cta<U, C, R>(x, res, w, q, s, T, H, G, eps, st);
+    const bool v8 = aligned(x, 32) && aligned(q, 32) && aligned(w, 32) && (!res || aligned(res, 32));
+#define FP8Q_ROW(NG)                                                                             \
+    (v8 ? launch_rms_row<NG, U, C, R, true>(x, res, w, q, s, T, H, G, eps, st)                  \
+        : launch_rms_row<NG, U, C, R, false>(x, res, w, q, s, T, H, G, eps, st))
+    if (G <= 64)
+        return FP8Q_ROW(1);
+    if (G <= 128)
+        return FP8Q_ROW(2);
+    return FP8Q_ROW(4);
+#undef FP8Q_ROW
 }
 
 }  // namespace

@@ -71,6 +71,22 @@ __device__ __forceinline__ void ld64_keep(const void *p, uint32_t (&w)[16])
     }
 }
 
+// 64 bytes every CTA of a SM reads (the RMSNorm weight): read-only path,
+// cached in L1.
+template <bool V8>
+__device__ __forceinline__ void ld64_keep_l1(const void *p, uint32_t (&w)[16])
+{
+    const char *c = static_cast<const char *>(p);
+    if (V8) {
+        FP8Q_LD8(".nc.L2::evict_last", c, w, 0);
+        FP8Q_LD8(".nc.L2::evict_last", c + 32, w, 8);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            FP8Q_LD4(".nc", c + 16 * k, w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+    }
+}
+
 // 64 bytes this kernel also writes (the residual): coherent path.
 template <bool V8>
 __device__ __forceinline__ void ld64_rw(const void *p, uint32_t (&w)[16])

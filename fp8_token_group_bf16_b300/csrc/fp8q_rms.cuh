@@ -108,16 +108,30 @@ __device__ __forceinline__ float rms_inv(float hi, float lo, int H, float eps)
 __device__ __forceinline__ uint32_t w_swizzle(uint32_t line) { return (((line >> 3) & 3u) << 1) | (line & 1u); }
 
 // All threads of the CTA; the caller synchronises before the first read.
+// Each thread issues four 16-byte loads before it converts and stores any,
+// so the table costs about one L2 round trip per four chunks of a thread.
 __device__ __forceinline__ void fill_weight_table(const uint16_t *__restrict__ w, int H, uint32_t wsm)
 {
-    for (int c = threadIdx.x; c < H / 8; c += blockDim.x) {
-        uint32_t p[4];
-        FP8Q_LD4(".nc", w + 8 * c, p[0], p[1], p[2], p[3]);
-        const uint32_t line = uint32_t(c) >> 2, k = uint32_t(c) & 3u, swz = w_swizzle(line);
-        const uint32_t lo[4] = {p[0] << 16, p[0] & 0xFFFF0000u, p[1] << 16, p[1] & 0xFFFF0000u};
-        const uint32_t hi[4] = {p[2] << 16, p[2] & 0xFFFF0000u, p[3] << 16, p[3] & 0xFFFF0000u};
-        sts128(wsm + line * 128u + ((2u * k) ^ swz) * 16u, lo);
-        sts128(wsm + line * 128u + ((2u * k + 1u) ^ swz) * 16u, hi);
+    const int n = H / 8;   // 16-byte chunks of 8 values
+    for (int c0 = threadIdx.x; c0 < n; c0 += 4 * blockDim.x) {
+        uint32_t p[4][4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int c = c0 + u * int(blockDim.x);
+            const int cc = c < n ? c : n - 1;   // clamped into the weight
+            FP8Q_LD4(".nc", w + 8 * cc, p[u][0], p[u][1], p[u][2], p[u][3]);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int c = c0 + u * int(blockDim.x);
+            if (c < n) {
+                const uint32_t line = uint32_t(c) >> 2, k = uint32_t(c) & 3u, swz = w_swizzle(line);
+                const uint32_t lo[4] = {p[u][0] << 16, p[u][0] & 0xFFFF0000u, p[u][1] << 16, p[u][1] & 0xFFFF0000u};
+                const uint32_t hi[4] = {p[u][2] << 16, p[u][2] & 0xFFFF0000u, p[u][3] << 16, p[u][3] & 0xFFFF0000u};
+                sts128(wsm + line * 128u + ((2u * k) ^ swz) * 16u, lo);
+                sts128(wsm + line * 128u + ((2u * k + 1u) ^ swz) * 16u, hi);
+            }
+        }
     }
 }
 
@@ -337,6 +351,108 @@ __global__ void __launch_bounds__(kRmsMaxThreads, 2) rms_warp_kernel(
         raise_device_error(kErrBarrierTimeout);
         for (int j = 0; j < nseg; ++j)   // the current row's copies: let them land first
             mbar_wait(bars + 8u * j, uint32_t(k) & 1u);
+    }
+}
+
+// -------------------------------------- CTA per row, row in registers ---
+//
+// One CTA per row (grid = T), one quad per group (NG groups per quad for
+// rows of more than 64 groups): every lane loads its 32 * NG values and its
+// 32 * NG weights straight into registers with 256-bit loads (128-bit when
+// the buffers are only 16-byte aligned), so the row is read from HBM once and
+// stays in registers between the sum of squares and the quantisation.  Each
+// warp reduces its lanes' exact partial sums with a butterfly; one barrier
+// joins the warps.  The weight is read through L1 (every CTA of a SM reads
+// the same bytes).  Short-lived CTAs at ~64 registers leave room for six per
+// SM, whose loads overlap the others' arithmetic.
+
+template <int NG, bool UE8M0, bool COL, bool RES, bool V8>
+__global__ void __launch_bounds__(kRmsMaxThreads, NG == 1 ? 4 : (NG == 2 ? 2 : 1)) rms_row_kernel(
+    const uint16_t *__restrict__ x, uint16_t *__restrict__ residual, const uint16_t *__restrict__ w,
+    uint8_t *__restrict__ q, float *__restrict__ scales, int T, int H, int G, float eps)
+{
+    __shared__ float2 red[kRmsMaxThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, sub = tid & 3, quad = tid >> 2, warp = tid >> 5;
+    const int nq = blockDim.x >> 2, nwarps = blockDim.x >> 5;
+    const int row = blockIdx.x;
+    const int64_t rbase = int64_t(row) * H;
+
+    wait_for_producer();
+    allow_consumer_launch();
+
+    uint32_t z[NG][16], wr[NG][16];
+#pragma unroll
+    for (int j = 0; j < NG; ++j) {
+        const int g = quad + nq * j;
+        const int off = (g < G ? g : G - 1) * kGroup + sub * kValsPerLane;   // clamped into the row
+        ld64_stream<V8>(x + rbase + off, z[j]);
+        if (RES) {
+            uint32_t r[16];
+            ld64_rw<V8>(residual + rbase + off, r);
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                z[j][e] = pack_bf16x2(__fadd_rn(bf_lo(z[j][e]), bf_lo(r[e])), __fadd_rn(bf_hi(z[j][e]), bf_hi(r[e])));
+        }
+        ld64_keep_l1<V8>(w + off, wr[j]);
+    }
+    if (RES) {
+#pragma unroll
+        for (int j = 0; j < NG; ++j) {
+            const int g = quad + nq * j;
+            if (g < G)
+                st64<V8>(residual + rbase + g * kGroup + sub * kValsPerLane, z[j]);
+        }
+    }
+
+    // ---- pass 1: exact sum of squares
+    float hi = 0.0f, lo = 0.0f;
+#pragma unroll
+    for (int j = 0; j < NG; ++j) {
+        float h, l;
+        lane_sumsq(z[j], h, l);
+        const bool act = quad + nq * j < G;
+        pair_add(hi, lo, act ? h : 0.0f, act ? l : 0.0f);
+    }
+#pragma unroll
+    for (int o = 1; o <= 16; o <<= 1)
+        pair_add(hi, lo, __shfl_xor_sync(0xFFFFFFFFu, hi, o), __shfl_xor_sync(0xFFFFFFFFu, lo, o));
+    if (lane == 0)
+        red[warp] = make_float2(hi, lo);
+    __syncthreads();
+    float2 a = red[0];
+    for (int i = 1; i < nwarps; ++i)   // every thread, in the same order
+        pair_add(a.x, a.y, red[i].x, red[i].y);
+    const float inv = rms_inv(a.x, a.y, H, eps);
+    const uint64_t inv2 = f2_pack(inv, inv);
+
+    // ---- pass 2: v = (z * inv) * w, group scale, codes
+#pragma unroll
+    for (int j = 0; j < NG; ++j) {
+        const int g = quad + nq * j;
+        uint64_t v[4][4];
+        float mm[2] = {0.0f, 0.0f};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int k = 4 * i + e;
+                v[i][e] = f2_mul(f2_mul(f2_from_bf16x2(z[j][k]), inv2), f2_from_bf16x2(wr[j][k]));
+                float va, vb;
+                f2_unpack(v[i][e], va, vb);
+                mm[e & 1] = absmax3(mm[e & 1], va, vb);
+            }
+        const float amax = quad_max(fmaxf(mm[0], mm[1]));
+        const float sc = group_scale<UE8M0>(amax, kScaleFloor);
+        const float rc = scale_recip<UE8M0>(sc);
+        uint32_t codes[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            quant8<UE8M0>(v[i], sc, rc, codes[2 * i], codes[2 * i + 1]);
+        if (g < G) {
+            st32<V8>(q + rbase + g * kGroup + sub * kValsPerLane, codes);
+            if (sub == 0)
+                scales[COL ? int64_t(g) * T + row : int64_t(row) * G + g] = sc;
+        }
     }
 }
 
