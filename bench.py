@@ -50,7 +50,7 @@ FALLBACK_HBM_GBS = 6400.0
 DOMINANT = "silu_and_mul_per_block_quant"
 KERNEL_NAMES = {   # the kernel each op launches at the step's T
     "per_token_group_fp8_quant": "group_quant_kernel",
-    "rms_norm_per_block_quant": "rms_warp_kernel",
+    "rms_norm_per_block_quant": "rms_row_kernel",
     "silu_and_mul_per_block_quant": "silu_quant_kernel",
 }
 

@@ -33,7 +33,6 @@ FP8Q_ERR_CUDA = 4
 FP8Q_SCALES_ROW_MAJOR = 0
 FP8Q_SCALES_COL_MAJOR = 1
 FP8Q_RMS_MAX_H = 32768
-FP8Q_RMS_MAX_H_RESIDUAL = 16384
 GROUP = 128
 
 EXPORTS = (
@@ -43,7 +42,6 @@ EXPORTS = (
     "fp8q_f32_to_e4m3",
     "fp8q_status_string",
     "fp8q_version",
-    "fp8q_take_device_error",
 )
 
 _lib = None
@@ -76,8 +74,6 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.fp8q_status_string.restype = ctypes.c_char_p
     L.fp8q_version.argtypes = []
     L.fp8q_version.restype = ctypes.c_int
-    L.fp8q_take_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
-    L.fp8q_take_device_error.restype = ctypes.c_int
     _lib = L
     return L
 
@@ -112,17 +108,6 @@ def fp8q_status_string(status: int) -> str:
 
 def fp8q_version() -> int:
     return load().fp8q_version()
-
-
-FP8Q_DEVICE_ERR_TIMEOUT = 1
-
-
-def fp8q_take_device_error() -> int:
-    """Synchronise the device and return (and clear) the device error flags;
-    raises if the device cannot be read."""
-    flags = ctypes.c_uint32(0)
-    _check(load().fp8q_take_device_error(ctypes.byref(flags)), "fp8q_take_device_error")
-    return int(flags.value)
 
 
 # ------------------------------------------------ tensor-level calls ----

@@ -7,7 +7,6 @@
 #include <cmath>
 #include <cstdint>
 #include <cuda_runtime.h>
-#include <mutex>
 
 namespace {
 
@@ -51,27 +50,16 @@ int launch_status(cudaError_t launched)
     return (launched == cudaSuccess && last == cudaSuccess) ? FP8Q_OK : FP8Q_ERR_CUDA;
 }
 
-// Number of SMs of the current device (148 on B300); 1 if it cannot be read.
-int sm_count()
-{
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-        return 1;
-    return n;
-}
-
 // Launch with programmatic stream serialization allowed: the kernel may be
 // scheduled while its predecessor on the stream drains, and waits for it
 // (griddepcontrol.wait) before touching global memory.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_smem(void (*kernel)(KArgs...), dim3 grid, dim3 block, uint32_t smem, cudaStream_t st,
-                        Args... args)
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t st, Args... args)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
 #ifndef FP8Q_NO_PDL
     cudaLaunchAttribute attr[1];
@@ -82,69 +70,6 @@ cudaError_t launch_smem(void (*kernel)(KArgs...), dim3 grid, dim3 block, uint32_
 #endif
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
-
-template <typename... KArgs, typename... Args>
-cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t st, Args... args)
-{
-    return launch_smem(kernel, grid, block, 0u, st, args...);
-}
-
-// Launch shapes depend only on the device, the kernel and the row length;
-// they are computed once (occupancy queries cost microseconds of host time)
-// and remembered in a small table shared by all host threads.
-struct ShapeCache {
-    struct Entry {
-        int dev;
-        const void *fn;
-        int H;
-        int a, b, c;
-    };
-    static constexpr int kEntries = 64;
-    std::mutex mu;
-    Entry e[kEntries];
-    int n = 0, next = 0;
-
-    bool find(int dev, const void *fn, int H, int &a, int &b, int &c)
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        for (int i = 0; i < n; ++i)
-            if (e[i].dev == dev && e[i].fn == fn && e[i].H == H) {
-                a = e[i].a, b = e[i].b, c = e[i].c;
-                return true;
-            }
-        return false;
-    }
-    void put(int dev, const void *fn, int H, int a, int b, int c)
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        const int i = n < kEntries ? n++ : (next++ % kEntries);
-        e[i] = Entry{dev, fn, H, a, b, c};
-    }
-};
-
-ShapeCache &shape_cache()
-{
-    static ShapeCache cache;
-    return cache;
-}
-
-int current_device()
-{
-    int dev = 0;
-    return cudaGetDevice(&dev) == cudaSuccess ? dev : -1;
-}
-
-// Dynamic shared memory above 48 KiB must be enabled per kernel and device.
-template <typename K>
-cudaError_t allow_smem(K kernel, uint32_t bytes)
-{
-    if (bytes <= 48u * 1024u)
-        return cudaSuccess;
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
-}
-
-// Largest dynamic shared memory a CTA may use on sm_100-class parts.
-constexpr uint32_t kSmemPerCtaMax = 227u * 1024u;
 
 template <bool U, bool C, bool V>
 cudaError_t launch_group(const uint16_t *x, uint8_t *q, float *s, int64_t n, int64_t G, int64_t T,
@@ -162,115 +87,6 @@ cudaError_t launch_silu(const uint16_t *x, uint8_t *q, float *s, int64_t n, int6
     return launch(silu_quant_kernel<U, C, V>, dim3{unsigned((n + kGroupsPerCta - 1) / kGroupsPerCta)},
                   dim3{unsigned(kCtaThreads)}, st, x, q, s, n, G, T, I, eps);
 }
-
-// rms_norm_per_block_quant, one CTA per row: at least three row stages with
-// four CTAs per SM if they fit, else at least two with three or two CTAs per
-// SM, else one CTA with whatever fits; within a budget, as many stages (up to
-// 8) as fit.
-int rms_cta_stages(int H, bool res)
-{
-    const struct {
-        uint32_t budget;
-        int min_stages;
-    } tiers[] = {{55u * 1024u, 3}, {72u * 1024u, 2}, {110u * 1024u, 2}, {kSmemPerCtaMax, 1}};
-    for (const auto &t : tiers)
-        for (int S = kRmsMaxStages; S >= t.min_stages; --S)
-            if (RmsCtaSmem(H, res, S).total <= t.budget)
-                return S;
-    return 0;
-}
-
-// one quad per group, up to 64 groups (longer rows loop over the groups)
-int rms_cta_threads(int G) { return G >= kRmsMaxThreads / 4 ? kRmsMaxThreads : ((G + 7) / 8) * 32; }
-
-template <bool U, bool C, bool R>
-cudaError_t launch_rms_cta(const uint16_t *x, uint16_t *res, const uint16_t *w, uint8_t *q, float *s,
-                           int T, int H, int G, float eps, cudaStream_t st)
-{
-    auto kernel = rms_cta_kernel<U, C, R>;
-    const int dev = current_device();
-    int S = 0, per_sm = 0, unused = 0;
-    if (!shape_cache().find(dev, reinterpret_cast<const void *>(kernel), H, S, per_sm, unused)) {
-        S = rms_cta_stages(H, R);
-        if (S < 1)
-            return cudaErrorInvalidValue;
-        const uint32_t smem = RmsCtaSmem(H, R, S).total;
-        // the cap is raised once to the largest shape; each launch asks for its own size
-        cudaError_t e = allow_smem(kernel, kSmemPerCtaMax);
-        if (e != cudaSuccess)
-            return e;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, rms_cta_threads(G), smem) != cudaSuccess ||
-            per_sm < 1) {
-            cudaGetLastError();
-            per_sm = 1;
-        }
-        shape_cache().put(dev, reinterpret_cast<const void *>(kernel), H, S, per_sm, 0);
-    }
-    const uint32_t smem = RmsCtaSmem(H, R, S).total;
-    const int64_t resident = int64_t(per_sm) * sm_count();
-    const int grid = int(T < resident ? T : resident);
-    return launch_smem(kernel, dim3{unsigned(grid)}, dim3{unsigned(rms_cta_threads(G))}, smem, st, x, res, w, q, s,
-                       T, H, G, eps, S);
-}
-
-// rms_norm_per_block_quant, one warp per row: the warps per CTA that give the
-// most resident warps per SM (each warp holds one row stage).
-struct WarpShape {
-    int warps = 0, per_sm = 0;
-};
-
-template <typename K>
-WarpShape rms_warp_shape(K kernel, int H, bool res)
-{
-    WarpShape best;
-    if (allow_smem(kernel, kSmemPerCtaMax) != cudaSuccess) {
-        cudaGetLastError();
-        return best;
-    }
-    for (int W : {8, 6, 4, 2}) {
-        const uint32_t smem = RmsWarpSmem(H, res, W).total;
-        if (smem > kSmemPerCtaMax)
-            continue;
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 32 * W, smem) != cudaSuccess)
-            continue;
-        if (per_sm * W > best.per_sm * best.warps) {
-            best.warps = W;
-            best.per_sm = per_sm;
-        }
-    }
-    cudaGetLastError();
-    return best;
-}
-
-template <bool U, bool C, bool R>
-cudaError_t launch_rms_warp(const uint16_t *x, uint16_t *res, const uint16_t *w, uint8_t *q, float *s, int T,
-                            int H, int G, float eps, cudaStream_t st, bool &launched)
-{
-    auto kernel = rms_warp_kernel<U, C, R>;
-    const int dev = current_device();
-    WarpShape ws;
-    int unused = 0;
-    if (!shape_cache().find(dev, reinterpret_cast<const void *>(kernel), H, ws.warps, ws.per_sm, unused)) {
-        ws = rms_warp_shape(kernel, H, R);
-        shape_cache().put(dev, reinterpret_cast<const void *>(kernel), H, ws.warps, ws.per_sm, 0);
-    }
-    launched = ws.warps > 0 && ws.warps * ws.per_sm >= 4;
-    if (!launched)
-        return cudaSuccess;
-    int64_t grid = int64_t(ws.per_sm) * sm_count();
-    const int64_t need = (T + ws.warps - 1) / ws.warps;
-    if (need < grid)
-        grid = need;
-    const uint32_t smem = RmsWarpSmem(H, R, ws.warps).total;
-    return launch_smem(kernel, dim3{unsigned(grid)}, dim3{unsigned(32 * ws.warps)}, smem, st, x, res, w, q, s, T, H,
-                       G, eps);
-}
-
-// Rows per launch from which the warp-per-row kernel takes over: below it a
-// row's latency, not the bytes, decides, and a CTA spreads a row over up to
-// 64 quads.
-constexpr int kRmsWarpMinRows = 1024;
 
 // rms_norm_per_block_quant, one CTA per row with the row in registers: one
 // quad per group up to 64 groups, 2 or 4 groups per quad beyond.
@@ -377,7 +193,7 @@ int fp8q_rms_norm_per_block_quant(const void *x, void *residual, const void *wei
         return rc;
     if (!std::isfinite(eps) || eps < 0.0f)
         return FP8Q_ERR_INVALID_ARG;
-    if (H > (residual ? FP8Q_RMS_MAX_H_RESIDUAL : FP8Q_RMS_MAX_H))
+    if (H > FP8Q_RMS_MAX_H)
         return FP8Q_ERR_UNSUPPORTED;
     if (T == 0)
         return FP8Q_OK;
@@ -437,20 +253,7 @@ const char *fp8q_status_string(int status)
     }
 }
 
-int fp8q_version(void) { return 300; }
+int fp8q_version(void) { return 400; }
 
-int fp8q_take_device_error(uint32_t *flags)
-{
-    if (!flags)
-        return FP8Q_ERR_INVALID_ARG;
-    uint32_t v = 0;
-    const uint32_t zero = 0;
-    if (cudaDeviceSynchronize() != cudaSuccess ||
-        cudaMemcpyFromSymbol(&v, fp8q::g_device_error, sizeof v) != cudaSuccess ||
-        cudaMemcpyToSymbol(fp8q::g_device_error, &zero, sizeof zero) != cudaSuccess)
-        return FP8Q_ERR_CUDA;
-    *flags = v;
-    return FP8Q_OK;
-}
 
 }  // extern "C"

@@ -67,10 +67,9 @@ typedef enum {
     FP8Q_SCALES_COL_MAJOR = 1  /* s[g*T + t] */
 } fp8q_scale_layout;
 
-/* Longest rms_norm_per_block_quant row (H) the kernels accept: a row, its
- * residual row and the weight (as fp32) are held in shared memory. */
+/* Longest rms_norm_per_block_quant row (H) the kernels accept (a row is held
+ * in the registers of one CTA). */
 #define FP8Q_RMS_MAX_H 32768
-#define FP8Q_RMS_MAX_H_RESIDUAL 16384
 
 /*
  * per_token_group_fp8_quant.
@@ -104,12 +103,8 @@ FP8Q_API int fp8q_per_token_group_quant(const void *x, void *q, float *scales, i
  * RN32(RN32(ss/H) + eps)))); v_h = RN32(RN32(z_h * inv) * w_h); then the
  * group quantisation of v.  Outside the underflow case the result is
  * therefore the same, bit for bit, as a sequential evaluation of these steps
- * with the sum carried in double precision.  H <= FP8Q_RMS_MAX_H
- * (FP8Q_RMS_MAX_H_RESIDUAL with a residual), else FP8Q_ERR_UNSUPPORTED;
- * T < 2^30.  Rows are staged in shared memory by bulk asynchronous copies;
- * a kernel that waited more than about a second for one gives up, leaves the
- * remaining rows unwritten and sets FP8Q_DEVICE_ERR_TIMEOUT (see
- * fp8q_take_device_error).
+ * with the sum carried in double precision.  H <= FP8Q_RMS_MAX_H and
+ * T < 2^30, else FP8Q_ERR_UNSUPPORTED.
  */
 FP8Q_API int fp8q_rms_norm_per_block_quant(const void *x, void *residual, const void *weight, void *q,
                                   float *scales, int64_t T, int64_t H, int32_t group_size,
@@ -136,17 +131,6 @@ FP8Q_API int fp8q_silu_and_mul_per_block_quant(const void *x, void *q, float *sc
  * aligned.  Exposed so the rounding can be checked on its own.
  */
 FP8Q_API int fp8q_f32_to_e4m3(const float *v, void *out, int64_t n, void *stream);
-
-/*
- * Device-side error flags, set by a kernel that stopped early (it gave up
- * waiting on a shared-memory barrier after about one second).  Bits:
- * FP8Q_DEVICE_ERR_TIMEOUT.  The call synchronises the current device, stores
- * the flags raised since the previous call into *flags, and clears them.
- * Returns FP8Q_ERR_INVALID_ARG for a NULL flags, FP8Q_ERR_CUDA if the device
- * cannot be synchronised or read (for example after a fault).
- */
-#define FP8Q_DEVICE_ERR_TIMEOUT 1u
-FP8Q_API int fp8q_take_device_error(uint32_t *flags);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 FP8Q_API const char *fp8q_status_string(int status);

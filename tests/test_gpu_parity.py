@@ -190,8 +190,6 @@ def test_rms_qwen3_mix(T):
                                  (3, 24576), (2, 32768), (300, 256), (700, 8192), (1, 8320)])
 @pytest.mark.parametrize("residual", [False, True], ids=["plain", "residual"])
 def test_rms_ragged_shapes(T, H, residual):
-    if residual and H > 16384:
-        pytest.skip("rows with a residual are limited to 16384 values (FP8Q_ERR_UNSUPPORTED, tested on CPU)")
     x, w, r = inputs.rms_input(T, H, seeds=(900 + T, 901 + H, 902))
     for ue8m0, col in VARIANTS:
         _check_rms(inputs.bits(x), inputs.bits(w), inputs.bits(r) if residual else None, ue8m0, col,
@@ -305,20 +303,11 @@ def test_rms_bit_exact_shapes(T, H):
     assert_exact(q, s, qr, sr, f"rms T={T} H={H}")
 
 
-def test_no_device_error_raised():
-    import fp8_token_group_bf16_b300 as fq
-
-    x, w, r = inputs.rms_input(64, 5120)
-    gpu_rms(inputs.bits(x), inputs.bits(w), inputs.bits(r), True, True)
-    gpu_silu(inputs.bits(inputs.silu_input(8, 1024)), True, False)
-    gpu_group_quant(inputs.bits(inputs.small_group_quant_input()))
-    assert fq.fp8q_take_device_error() == 0
-
-
 @pytest.mark.parametrize("T,H,residual", [(1100, 4096, True), (1024, 5120, False), (2048, 8192, True),
-                                          (1500, 384, True), (1031, 1152, False)])
+                                          (1500, 384, True), (1031, 1152, False), (64, 16384, True),
+                                          (33, 12288, False), (9, 32768, True), (17, 20480, False)])
 def test_rms_many_rows_bit_exact(T, H, residual):
-    """Launches of 1024 rows or more take the warp-per-row kernel."""
+    """Larger launches, ragged group counts, and rows of 1, 2 and 4 groups per quad."""
     x, w, r = inputs.rms_input(T, H, seeds=(910 + T, 911 + H, 912))
     xb, wb, rb = inputs.bits(x), inputs.bits(w), inputs.bits(r) if residual else None
     for ue8m0, col in VARIANTS:

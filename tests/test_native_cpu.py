@@ -98,8 +98,7 @@ def test_unsupported(lib):
     assert fq.fp8q_rms_norm_per_block_quant(A, None, A, Q, S, 4, 512, 256, 1e-6, 0, 0, None) == U
     assert fq.fp8q_rms_norm_per_block_quant(A, None, A, Q, S, 4, fq.FP8Q_RMS_MAX_H + 128, 128, 1e-6,
                                             0, 0, None) == U
-    # with a residual the row, its residual row and the fp32 weight share shared memory
-    assert fq.fp8q_rms_norm_per_block_quant(A, A + 64, A, Q, S, 4, fq.FP8Q_RMS_MAX_H_RESIDUAL + 128, 128,
+    assert fq.fp8q_rms_norm_per_block_quant(A, A + 64, A, Q, S, 4, fq.FP8Q_RMS_MAX_H + 128, 128,
                                             1e-6, 0, 0, None) == U
 
 
