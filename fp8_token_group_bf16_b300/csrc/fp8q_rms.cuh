@@ -2,7 +2,7 @@
 // held in registers, an error-free row sum of squares, then the group
 // quantisation of the normalised row.
 //
-// Sum of squares.  A lane seeds four accumulators (two packed pairs) with
+// Sum of squares.  A lane seeds two accumulators (one packed pair) with
 // pm = the largest square among its 32 values and adds the squares (each
 // exact in fp32: a bf16 value has 8 significant bits) with Dekker's Fast2Sum,
 // whose precondition |accumulator| >= |addend| the seed guarantees; the
@@ -23,8 +23,7 @@ constexpr int kRmsMaxThreads = 256;
 
 // Squares of one lane's 32 values (16 bf16x2 words), summed exactly:
 // returns (hi, lo) with hi + lo equal to the sum up to lo's own rounding.
-// Four accumulators (two packed pairs: even and odd words) shorten the
-// dependency chains.
+// The two halves of the packed pair accumulate the even and the odd values.
 __device__ __forceinline__ void lane_sumsq(const uint32_t (&w)[16], float &hi, float &lo)
 {
     float m0 = 0.0f, m1 = 0.0f;
@@ -35,35 +34,28 @@ __device__ __forceinline__ void lane_sumsq(const uint32_t (&w)[16], float &hi, f
     }
     const float m = fmaxf(m0, m1);
     const float pm = __fmul_rn(m, m);
-    uint64_t s[2] = {f2_pack(pm, pm), f2_pack(pm, pm)};
-    uint64_t c[2] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f)};
+    uint64_t s = f2_pack(pm, pm);
+    uint64_t c = f2_pack(0.0f, 0.0f);
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-        const int a = k & 1;
         const uint64_t z = f2_from_bf16x2(w[k]);
         const uint64_t p = f2_mul(z, z);
-        const uint64_t t = f2_add(s[a], p);
-        c[a] = f2_add(c[a], f2_sub(p, f2_sub(t, s[a])));   // Fast2Sum error, |s| >= |p|
-        s[a] = t;
+        const uint64_t t = f2_add(s, p);
+        c = f2_add(c, f2_sub(p, f2_sub(t, s)));   // Fast2Sum error, |s| >= |p|
+        s = t;
     }
-    float sv[4], cv[4];
-    f2_unpack(s[0], sv[0], sv[1]);
-    f2_unpack(s[1], sv[2], sv[3]);
-    f2_unpack(c[0], cv[0], cv[1]);
-    f2_unpack(c[1], cv[2], cv[3]);
+    float sv[2], cv[2];
+    f2_unpack(s, sv[0], sv[1]);
+    f2_unpack(c, cv[0], cv[1]);
     const float inf = __int_as_float(0x7F800000);
-    if (!(sv[0] < inf && sv[1] < inf && sv[2] < inf && sv[3] < inf)) {   // the squares overflow fp32:
-        hi = inf;                                                         // so does the row sum
+    if (!(sv[0] < inf && sv[1] < inf)) {
+        hi = inf;
         lo = 0.0f;
         return;
     }
-    // each accumulator minus its seed is exact; combine the four without error
-    float h01, e01, h23, e23;
-    two_sum(__fsub_rn(sv[0], pm), __fsub_rn(sv[1], pm), h01, e01);
-    two_sum(__fsub_rn(sv[2], pm), __fsub_rn(sv[3], pm), h23, e23);
     float e;
-    two_sum(h01, h23, hi, e);
-    lo = __fadd_rn(__fadd_rn(__fadd_rn(cv[0], cv[1]), __fadd_rn(cv[2], cv[3])), __fadd_rn(__fadd_rn(e01, e23), e));
+    two_sum(__fsub_rn(sv[0], pm), __fsub_rn(sv[1], pm), hi, e);
+    lo = __fadd_rn(__fadd_rn(cv[0], cv[1]), e);
 }
 
 // inv = RN32(1 / RN32(sqrt(RN32(RN32(ss / H) + eps)))) with ss = RN32(hi + lo).
