@@ -100,6 +100,8 @@ def _configure(L: ctypes.CDLL) -> ctypes.CDLL:
     for name in ("oracle_per_token_group_quant", "oracle_rms_norm_per_block_quant",
                  "oracle_silu_and_mul_per_block_quant"):
         getattr(L, name).restype = I
+    L.oracle_pack_ue8m0.argtypes = [P, I64, I64, P]
+    L.oracle_pack_ue8m0.restype = I
     L.oracle_f32_to_e4m3_n.argtypes = [P, P, I64]
     L.oracle_ue8m0_ceil_n.argtypes = [P, P, I64]
     L.oracle_silu_mul_n.argtypes = [P, P, P, I64]
@@ -187,6 +189,17 @@ def silu_and_mul_per_block_quant(x_bits, group=128, eps=SCALE_EPS, ue8m0=False, 
     if want_values:
         return q, s, sp, v
     return q, s, sp
+
+
+def pack_ue8m0(scales_tg) -> np.ndarray:
+    """Power-of-two scales [T, G] (fp32, row-major) -> the packed UE8M0 bytes
+    (layout in fp8q_oracle.c), as a uint8 array [ceil(G/4), round_up(T, 4), 4]."""
+    s = np.ascontiguousarray(scales_tg, dtype=np.float32)
+    T, G = s.shape
+    K, T_pad = -(-G // 4), -(-T // 4) * 4
+    out = np.empty((K, T_pad, 4), np.uint8)
+    _check(lib().oracle_pack_ue8m0(_p(s), T, G, _p(out)))
+    return out
 
 
 def f32_to_e4m3(v) -> np.ndarray:

@@ -334,6 +334,39 @@ int oracle_silu_and_mul_per_block_quant(const uint16_t *x, uint8_t *q, float *sc
     return ORACLE_OK;
 }
 
+/* ---------------------------------------------- packed UE8M0 scales -- */
+
+/*
+ * Power-of-two ("ceiling E8M0") scales as the 8-bit exponents that block-
+ * scaled FP8 GEMMs on Blackwell read: an E8M0 byte b stands for 2^(b - 127).
+ * Layout: 32-bit words, token-major in the fast dimension and four groups per
+ * word: word (k, t), k < ceil(G/4), t < T_pad = T rounded up to a multiple
+ * of 4, lives at word index k * T_pad + t, and its byte j (little-endian,
+ * j = 0..3) is the exponent of group 4k + j of token t.  Bytes of groups
+ * past G and of tokens past T are 0.  Input: the fp32 scales, row-major
+ * [T, G], each a power of two.  Output: ceil(G/4) * T_pad * 4 bytes.
+ */
+int oracle_pack_ue8m0(const float *scales_tg, int64_t T, int64_t G, uint8_t *out)
+{
+    if (T < 0 || G <= 0)
+        return ORACLE_ERR_ARG;
+    const int64_t T_pad = (T + 3) / 4 * 4;
+    const int64_t K = (G + 3) / 4;
+    memset(out, 0, (size_t)(K * T_pad * 4));
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t g = 0; g < G; ++g) {
+            float s = scales_tg[t * G + g];
+            int e;
+            float f = frexpf(s, &e); /* s = f * 2^e, f in [0.5, 1) */
+            if (f != 0.5f || e - 1 + 127 < 1 || e - 1 + 127 > 254)
+                return ORACLE_ERR_ARG; /* not a normal power of two */
+            int64_t word = (g / 4) * T_pad + t;
+            out[word * 4 + (g % 4)] = (uint8_t)(e - 1 + 127); /* s = 2^(e-1) */
+        }
+    }
+    return ORACLE_OK;
+}
+
 /* ----------------------------------------------- batch helpers (tests) -- */
 
 void oracle_f32_to_e4m3_n(const float *v, uint8_t *out, int64_t n)

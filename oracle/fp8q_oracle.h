@@ -55,6 +55,10 @@ int oracle_silu_and_mul_per_block_quant(const uint16_t *x, uint8_t *q, float *sc
                                         float *scales_pre, float *v_out, int64_t T, int64_t I,
                                         int64_t gs, float eps, int ue8m0, int col_major);
 
+/* Packed UE8M0 scales (layout in fp8q_oracle.c): scales_tg fp32 [T,G]
+ * row-major powers of two -> ceil(G/4) * round_up(T,4) * 4 bytes. */
+int oracle_pack_ue8m0(const float *scales_tg, int64_t T, int64_t G, uint8_t *out);
+
 void oracle_f32_to_e4m3_n(const float *v, uint8_t *out, int64_t n);
 void oracle_ue8m0_ceil_n(const float *s, float *out, int64_t n);
 void oracle_silu_mul_n(const float *a, const float *b, float *out, int64_t n);

@@ -337,6 +337,61 @@ def pin_scale_layouts():
     assert np.array_equal(ra[0], rb[0]) and np.array_equal(rb[1], ra[1].T)
 
 
+def load_packed_golden():
+    T = G = None
+    words = {}
+    with open(os.path.join(GOLDEN, "ue8m0_packed.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            parts = line.split()
+            if parts[0] == "T":
+                T = int(parts[1])
+            elif parts[0] == "G":
+                G = int(parts[1])
+            else:
+                k, t, *b = (int(v) for v in parts)
+                words[(k, t)] = b
+    return T, G, words
+
+
+def pin_ue8m0_packed_golden():
+    """The packing of a hand-derived example, byte for byte."""
+    T, G, words = load_packed_golden()
+    s = np.array([[2.0 ** (t - g) for g in range(G)] for t in range(T)], np.float32)
+    got = oracle.pack_ue8m0(s)
+    K, T_pad = -(-G // 4), -(-T // 4) * 4
+    assert got.shape == (K, T_pad, 4) and len(words) == K * T_pad
+    for (k, t), b in words.items():
+        assert got[k, t].tolist() == b, ((k, t), got[k, t].tolist(), b)
+
+
+def pin_ue8m0_packed_decodes():
+    """On op A's UE8M0 scales: every byte decodes to its scale exactly, the
+    pad bytes are 0, and the bytes are the scales' exponents as a multiset."""
+    for T, H in ((7, 896), (4, 512), (1, 7168)):
+        xb = inputs.bits(inputs.heavy_tailed_input(T, H, seed=60 + T))
+        _, s, _ = oracle.per_token_group_quant(xb, ue8m0=True)
+        G = H // 128
+        p = oracle.pack_ue8m0(s)
+        K, T_pad = -(-G // 4), -(-T // 4) * 4
+        assert p.shape == (K, T_pad, 4)
+        seen = []
+        for k in range(K):
+            for t in range(T_pad):
+                for j in range(4):
+                    g = 4 * k + j
+                    b = int(p[k, t, j])
+                    if t >= T or g >= G:
+                        assert b == 0, (k, t, j)
+                    else:
+                        assert math.ldexp(1.0, b - 127) == float(s[t, g]), (t, g, b, s[t, g])
+                        seen.append(b)
+        want = sorted(int(math.frexp(float(v))[1]) + 126 for v in s.reshape(-1))
+        assert sorted(seen) == want
+
+
 # ------------------------------------------------------- op B (rms) ----
 
 
@@ -574,6 +629,8 @@ def pin_silu_large_negative_gate():
 
 ALL_PINS = [
     pin_golden_midpoints,
+    pin_ue8m0_packed_golden,
+    pin_ue8m0_packed_decodes,
     pin_e4m3_roundtrip,
     pin_op_a_hand_rows,
     pin_scale_layouts,

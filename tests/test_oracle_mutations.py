@@ -78,6 +78,12 @@ MUTATIONS = {
         "float b = oracle_bf16_to_f32(xr[g * gs + i]);\n                float a = oracle_bf16_to_f32(xr[I + g * gs + i]);",
     ),
     "silu_up_row_stride_wrong": ("const uint16_t *xr = x + t * 2 * I;", "const uint16_t *xr = x + t * I;"),
+    "packed_byte_order_reversed": ("out[word * 4 + (g % 4)] = (uint8_t)(e - 1 + 127);",
+                                   "out[word * 4 + (3 - g % 4)] = (uint8_t)(e - 1 + 127);"),
+    "packed_stride_unpadded": ("int64_t word = (g / 4) * T_pad + t;", "int64_t word = (g / 4) * T + t;"),
+    "packed_exponent_unbiased_off_by_one": ("out[word * 4 + (g % 4)] = (uint8_t)(e - 1 + 127);",
+                                            "out[word * 4 + (g % 4)] = (uint8_t)(e + 127);"),
+    "packed_groups_fast": ("int64_t word = (g / 4) * T_pad + t;", "int64_t word = t * K + (g / 4);"),
     "rms_sumsq_missing_last": ("for (int64_t h = 0; h < H; ++h)\n            acc += ",
                                "for (int64_t h = 0; h < H - 1; ++h)\n            acc += "),
 }
