@@ -58,19 +58,22 @@ KERNEL_NAMES = {   # the kernel each op launches at the step's T
 # ------------------------------------------------------------------ bytes --
 
 
-def algorithmic_bytes(op: str, T: int, H: int, residual: bool = False) -> int:
+def algorithmic_bytes(op: str, T: int, H: int, residual: bool = False, packed: bool = False) -> int:
     """Bytes an op must move: each input read once, each output written once.
     group: x bf16 [T,H] in; e4m3 [T,H] and fp32 [T,H/128] out.
     rms:   the same plus the bf16 weight [H]; with the residual, the
            residual [T,H] is read and written (+4 B per element).
-    silu:  H is I; x bf16 [T,2I] in; e4m3 [T,I] and fp32 [T,I/128] out."""
+    silu:  H is I; x bf16 [T,2I] in; e4m3 [T,I] and fp32 [T,I/128] out.
+    packed: the scales are exponent bytes, [ceil(G/4), T rounded up to 4]
+           32-bit words, instead of fp32 [T, G]."""
     G = H // GROUP
+    sb = -(-G // 4) * (-(-T // 4) * 4) * 4 if packed else 4 * T * G
     if op == "per_token_group_fp8_quant":
-        return T * H * 3 + 4 * T * G
+        return T * H * 3 + sb
     if op == "rms_norm_per_block_quant":
-        return T * H * 3 + 4 * T * G + 2 * H + (4 * T * H if residual else 0)
+        return T * H * 3 + sb + 2 * H + (4 * T * H if residual else 0)
     if op == "silu_and_mul_per_block_quant":
-        return T * H * 5 + 4 * T * G
+        return T * H * 5 + sb
     raise ValueError(op)
 
 
@@ -587,38 +590,47 @@ def sweep(args):
         return make
 
     e4 = torch.float8_e4m3fn
-    points = []
+    points = []   # (op, T, H or I, ue8m0, scale layout, residual)
     for T in (1, 4, 16, 64, 256, 512, 1024, 4096, 16384):
-        for ue8m0, col in ((False, False), (True, True)):
-            points.append(("per_token_group_fp8_quant", T, A_H, ue8m0, col, False))
+        for ue8m0, lay in ((False, "row"), (True, "col")):
+            points.append(("per_token_group_fp8_quant", T, A_H, ue8m0, lay, False))
     for T in (1, 8, 64, 512, 4096, 16384):
-        points.append(("rms_norm_per_block_quant", T, B_H, True, False, False))
-        points.append(("silu_and_mul_per_block_quant", T, C_I, True, False, False))
-    points.append(("rms_norm_per_block_quant", 256, 4096, False, False, True))
-    points.append(("rms_norm_per_block_quant", 256, 4096, False, False, False))
-    points.append(("silu_and_mul_per_block_quant", 1024, 12288, True, True, False))
+        points.append(("rms_norm_per_block_quant", T, B_H, True, "row", False))
+        points.append(("silu_and_mul_per_block_quant", T, C_I, True, "row", False))
+    points.append(("rms_norm_per_block_quant", 256, 4096, False, "row", True))
+    points.append(("rms_norm_per_block_quant", 256, 4096, False, "row", False))
+    points.append(("silu_and_mul_per_block_quant", 1024, 12288, True, "col", False))
+    for T in (512, 4096):   # packed UE8M0 exponent bytes
+        points.append(("per_token_group_fp8_quant", T, A_H, True, "packed", False))
+        points.append(("rms_norm_per_block_quant", T, B_H, True, "packed", False))
+        points.append(("silu_and_mul_per_block_quant", T, C_I, True, "packed", False))
     rows = []
-    for op, T, H, ue8m0, col, res in points:
-        nbytes = algorithmic_bytes(op, T, H, res)
+    for op, T, H, ue8m0, lay, res in points:
+        nbytes = algorithmic_bytes(op, T, H, res, packed=lay == "packed")
         G = H // GROUP
 
-        def make(op=op, T=T, H=H, ue8m0=ue8m0, col=col, res=res, G=G):
+        def make(op=op, T=T, H=H, ue8m0=ue8m0, lay=lay, res=res, G=G):
             xin = torch.randn(T, 2 * H if op.startswith("silu") else H, device=dev).to(torch.bfloat16)
             q = torch.empty(T, H, dtype=e4, device=dev)
-            s = torch.empty(G, T, device=dev).t() if col else torch.empty(T, G, device=dev)
+            if lay == "packed":
+                s = torch.empty(fq.packed_scale_shape(T, G), dtype=torch.int32, device=dev)
+            else:
+                s = torch.empty(G, T, device=dev).t() if lay == "col" else torch.empty(T, G, device=dev)
+            kw = dict(ue8m0=ue8m0, column_major_scales=lay == "col", packed_ue8m0_scales=lay == "packed",
+                      q=q, scales=s)
             if op == "per_token_group_fp8_quant":
-                return lambda: fq.per_token_group_fp8_quant(xin, ue8m0=ue8m0, column_major_scales=col, q=q, scales=s)
+                return lambda: fq.per_token_group_fp8_quant(xin, **kw)
             if op == "silu_and_mul_per_block_quant":
-                return lambda: fq.silu_and_mul_per_block_quant(xin, ue8m0=ue8m0, column_major_scales=col, q=q, scales=s)
+                return lambda: fq.silu_and_mul_per_block_quant(xin, **kw)
             w = torch.randn(H, device=dev).to(torch.bfloat16)
             r = torch.randn(T, H, device=dev).to(torch.bfloat16) if res else None
-            return lambda: fq.rms_norm_per_block_quant(xin, w, r, ue8m0=ue8m0, column_major_scales=col, q=q, scales=s)
+            return lambda: fq.rms_norm_per_block_quant(xin, w, r, **kw)
 
         iters = 200 if nbytes < 50e6 else 40
         us = timed(make, nbytes, iters)
         cus = timed(copy_maker(nbytes), nbytes, iters)
         torch.cuda.empty_cache()
-        row = {"op": op, "T": T, "H_or_I": H, "ue8m0": ue8m0, "col_major": col, "residual": res,
+        row = {"op": op, "T": T, "H_or_I": H, "ue8m0": ue8m0, "scales": lay, "residual": res,
                "bytes": nbytes, "us": round(us, 3), "GBps": round(nbytes / us / 1e3, 1),
                "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "copy_us": round(cus, 3),
                "copy_GBps": round(nbytes / cus / 1e3, 1), "peak": peak, "peak_kind": peak_kind}

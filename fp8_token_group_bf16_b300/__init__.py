@@ -32,6 +32,7 @@ FP8Q_ERR_MISALIGNED = 3
 FP8Q_ERR_CUDA = 4
 FP8Q_SCALES_ROW_MAJOR = 0
 FP8Q_SCALES_COL_MAJOR = 1
+FP8Q_SCALES_UE8M0_PACKED = 2
 FP8Q_RMS_MAX_H = 32768
 GROUP = 128
 
@@ -141,47 +142,69 @@ def _need_cuda_bf16(name, t):
         raise ValueError(f"{name} must be contiguous")
 
 
-def _outputs(x, T, cols, group_size, column_major_scales, q, scales):
+def packed_scale_shape(T: int, G: int):
+    """Shape of packed UE8M0 scales as int32 words: [ceil(G/4), T rounded up to 4]."""
+    return (-(-G // 4), -(-T // 4) * 4)
+
+
+def _layout(column_major_scales, packed_ue8m0_scales, ue8m0):
+    if packed_ue8m0_scales:
+        if not ue8m0:
+            raise ValueError("packed UE8M0 scales need ue8m0=True")
+        return FP8Q_SCALES_UE8M0_PACKED
+    return FP8Q_SCALES_COL_MAJOR if column_major_scales else FP8Q_SCALES_ROW_MAJOR
+
+
+def _outputs(x, T, cols, group_size, layout, q, scales):
     torch = _torch()
     G = cols // group_size
     if q is None:
         q = torch.empty((T, cols), dtype=torch.float8_e4m3fn, device=x.device)
     if scales is None:
-        if column_major_scales:
+        if layout == FP8Q_SCALES_UE8M0_PACKED:
+            scales = torch.empty(packed_scale_shape(T, G), dtype=torch.int32, device=x.device)
+        elif layout == FP8Q_SCALES_COL_MAJOR:
             scales = torch.empty((G, T), dtype=torch.float32, device=x.device).t()
         else:
             scales = torch.empty((T, G), dtype=torch.float32, device=x.device)
     return q, scales
 
 
-def _scale_ptr(scales, T, G, column_major_scales):
-    want = (1, T) if column_major_scales else (G, 1)
+def _scale_ptr(scales, T, G, layout):
+    if layout == FP8Q_SCALES_UE8M0_PACKED:
+        if tuple(scales.shape) != packed_scale_shape(T, G) or scales.dtype != _torch().int32 or \
+                not scales.is_contiguous():
+            raise ValueError(f"packed scales must be a contiguous int32 tensor of shape {packed_scale_shape(T, G)}")
+        return scales.data_ptr()
+    want = (1, T) if layout == FP8Q_SCALES_COL_MAJOR else (G, 1)
     if tuple(scales.shape) != (T, G) or (T > 1 and G > 1 and tuple(scales.stride()) != want):
         raise ValueError(f"scales must be a [T, G] = [{T}, {G}] fp32 tensor with strides {want}")
     return scales.data_ptr()
 
 
 def per_token_group_fp8_quant(x, group_size: int = GROUP, eps: float = 1e-10, ue8m0: bool = False,
-                              column_major_scales: bool = False, q=None, scales=None, stream=None):
+                              column_major_scales: bool = False, q=None, scales=None, stream=None,
+                              packed_ue8m0_scales: bool = False):
     """x bf16 [T, H] (CUDA, contiguous) -> (q float8_e4m3fn [T, H], scales fp32 [T, H/g]).
 
-    Column-major scales come back as a [T, G] view of a [G, T] buffer."""
+    Column-major scales come back as a [T, G] view of a [G, T] buffer;
+    packed UE8M0 scales as int32 words [ceil(G/4), T rounded up to 4]."""
     _need_cuda_bf16("x", x)
     if x.dim() != 2:
         raise ValueError("x must be 2-D [T, H]")
     T, H = x.shape
-    q, scales = _outputs(x, T, H, group_size, column_major_scales, q, scales)
-    sp = _scale_ptr(scales, T, H // max(group_size, 1), column_major_scales)
+    layout = _layout(column_major_scales, packed_ue8m0_scales, ue8m0)
+    q, scales = _outputs(x, T, H, group_size, layout, q, scales)
+    sp = _scale_ptr(scales, T, H // max(group_size, 1), layout)
     _check(fp8q_per_token_group_quant(
-        x.data_ptr(), q.data_ptr(), sp, T, H, group_size, eps, int(ue8m0),
-        FP8Q_SCALES_COL_MAJOR if column_major_scales else FP8Q_SCALES_ROW_MAJOR,
+        x.data_ptr(), q.data_ptr(), sp, T, H, group_size, eps, int(ue8m0), layout,
         _stream_ptr(x, stream)), "per_token_group_fp8_quant")
     return q, scales
 
 
 def rms_norm_per_block_quant(x, weight, residual=None, eps: float = 1e-6, group_size: int = GROUP,
                              ue8m0: bool = False, column_major_scales: bool = False, q=None,
-                             scales=None, stream=None):
+                             scales=None, stream=None, packed_ue8m0_scales: bool = False):
     """RMSNorm(x [+ residual]) * weight, then group FP8 quantisation.
 
     When ``residual`` is given it is updated in place to bf16(x + residual),
@@ -195,29 +218,29 @@ def rms_norm_per_block_quant(x, weight, residual=None, eps: float = 1e-6, group_
     if x.dim() != 2 or weight.dim() != 1 or weight.shape[0] != x.shape[1]:
         raise ValueError("x must be [T, H] and weight [H]")
     T, H = x.shape
-    q, scales = _outputs(x, T, H, group_size, column_major_scales, q, scales)
-    sp = _scale_ptr(scales, T, H // max(group_size, 1), column_major_scales)
+    layout = _layout(column_major_scales, packed_ue8m0_scales, ue8m0)
+    q, scales = _outputs(x, T, H, group_size, layout, q, scales)
+    sp = _scale_ptr(scales, T, H // max(group_size, 1), layout)
     _check(fp8q_rms_norm_per_block_quant(
         x.data_ptr(), residual.data_ptr() if residual is not None else None, weight.data_ptr(),
-        q.data_ptr(), sp, T, H, group_size, eps, int(ue8m0),
-        FP8Q_SCALES_COL_MAJOR if column_major_scales else FP8Q_SCALES_ROW_MAJOR,
+        q.data_ptr(), sp, T, H, group_size, eps, int(ue8m0), layout,
         _stream_ptr(x, stream)), "rms_norm_per_block_quant")
     return q, scales
 
 
 def silu_and_mul_per_block_quant(x, group_size: int = GROUP, eps: float = 1e-10, ue8m0: bool = False,
                                  column_major_scales: bool = False, q=None, scales=None,
-                                 stream=None):
+                                 stream=None, packed_ue8m0_scales: bool = False):
     """x bf16 [T, 2I] = [gate | up] -> quant(silu(gate) * up): (q [T, I], scales [T, I/g])."""
     _need_cuda_bf16("x", x)
     if x.dim() != 2 or x.shape[1] % 2:
         raise ValueError("x must be [T, 2I]")
     T, I = x.shape[0], x.shape[1] // 2
-    q, scales = _outputs(x, T, I, group_size, column_major_scales, q, scales)
-    sp = _scale_ptr(scales, T, I // max(group_size, 1), column_major_scales)
+    layout = _layout(column_major_scales, packed_ue8m0_scales, ue8m0)
+    q, scales = _outputs(x, T, I, group_size, layout, q, scales)
+    sp = _scale_ptr(scales, T, I // max(group_size, 1), layout)
     _check(fp8q_silu_and_mul_per_block_quant(
-        x.data_ptr(), q.data_ptr(), sp, T, I, group_size, eps, int(ue8m0),
-        FP8Q_SCALES_COL_MAJOR if column_major_scales else FP8Q_SCALES_ROW_MAJOR,
+        x.data_ptr(), q.data_ptr(), sp, T, I, group_size, eps, int(ue8m0), layout,
         _stream_ptr(x, stream)), "silu_and_mul_per_block_quant")
     return q, scales
 

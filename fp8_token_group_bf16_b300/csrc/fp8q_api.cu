@@ -15,12 +15,15 @@ using namespace fp8q;
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int check_common(const void *x, const void *q, const float *scales, int64_t T, int64_t H,
-                 int32_t group_size, int32_t scale_layout)
+                 int32_t group_size, int32_t ue8m0, int32_t scale_layout)
 {
     if (T < 0 || H <= 0 || group_size <= 0 || H % group_size != 0)
         return FP8Q_ERR_INVALID_ARG;
-    if (scale_layout != FP8Q_SCALES_ROW_MAJOR && scale_layout != FP8Q_SCALES_COL_MAJOR)
+    if (scale_layout != FP8Q_SCALES_ROW_MAJOR && scale_layout != FP8Q_SCALES_COL_MAJOR &&
+        scale_layout != FP8Q_SCALES_UE8M0_PACKED)
         return FP8Q_ERR_INVALID_ARG;
+    if (scale_layout == FP8Q_SCALES_UE8M0_PACKED && !ue8m0)
+        return FP8Q_ERR_INVALID_ARG;   // exponent bytes hold powers of two only
     if (group_size != kGroup)
         return FP8Q_ERR_UNSUPPORTED;
     if (T == 0)
@@ -71,7 +74,7 @@ cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-template <bool U, bool C, bool V>
+template <bool U, int C, bool V>
 cudaError_t launch_group(const uint16_t *x, uint8_t *q, float *s, int64_t n, int64_t G, int64_t T,
                          float eps, cudaStream_t st)
 {
@@ -80,7 +83,7 @@ cudaError_t launch_group(const uint16_t *x, uint8_t *q, float *s, int64_t n, int
                   dim3{unsigned(kCtaThreads)}, st, x, q, s, n, G, T, eps);
 }
 
-template <bool U, bool C, bool V>
+template <bool U, int C, bool V>
 cudaError_t launch_silu(const uint16_t *x, uint8_t *q, float *s, int64_t n, int64_t G, int64_t T,
                         int64_t I, float eps, cudaStream_t st)
 {
@@ -90,7 +93,7 @@ cudaError_t launch_silu(const uint16_t *x, uint8_t *q, float *s, int64_t n, int6
 
 // rms_norm_per_block_quant, one CTA per row with the row in registers: one
 // quad per group up to 64 groups, 2 or 4 groups per quad beyond.
-template <int NG, bool U, bool C, bool R, bool V>
+template <int NG, bool U, int C, bool R, bool V>
 cudaError_t launch_rms_row(const uint16_t *x, uint16_t *res, const uint16_t *w, uint8_t *q, float *s, int T,
                            int H, int G, float eps, cudaStream_t st)
 {
@@ -100,7 +103,7 @@ cudaError_t launch_rms_row(const uint16_t *x, uint16_t *res, const uint16_t *w, 
                   T, H, G, eps);
 }
 
-template <bool U, bool C, bool R>
+template <bool U, int C, bool R>
 cudaError_t launch_rms(const uint16_t *x, uint16_t *res, const uint16_t *w, uint8_t *q, float *s,
                        int T, int H, int G, float eps, cudaStream_t st)
 {
@@ -124,7 +127,7 @@ int fp8q_per_token_group_quant(const void *x, void *q, float *scales, int64_t T,
                                int32_t group_size, float eps, int32_t ue8m0, int32_t scale_layout,
                                void *stream)
 {
-    int rc = check_common(x, q, scales, T, H, group_size, scale_layout);
+    int rc = check_common(x, q, scales, T, H, group_size, ue8m0, scale_layout);
     if (rc != FP8Q_OK)
         return rc;
     if (!valid_scale_eps(eps))
@@ -139,15 +142,18 @@ int fp8q_per_token_group_quant(const void *x, void *q, float *scales, int64_t T,
     auto xp = static_cast<const uint16_t *>(x);
     auto qp = static_cast<uint8_t *>(q);
     const bool col = scale_layout == FP8Q_SCALES_COL_MAJOR;
+    const bool packed = scale_layout == FP8Q_SCALES_UE8M0_PACKED;
     const bool v8 = aligned(x, 32) && aligned(q, 32);
     cudaError_t e;
 #define FP8Q_GROUP(U, C)                                                                         \
     (v8 ? launch_group<U, C, true>(xp, qp, scales, n, G, T, eps, st)                            \
         : launch_group<U, C, false>(xp, qp, scales, n, G, T, eps, st))
-    if (ue8m0)
-        e = col ? FP8Q_GROUP(true, true) : FP8Q_GROUP(true, false);
+    if (packed)
+        e = FP8Q_GROUP(true, kPackedUe8m0);
+    else if (ue8m0)
+        e = col ? FP8Q_GROUP(true, kColMajor) : FP8Q_GROUP(true, kRowMajor);
     else
-        e = col ? FP8Q_GROUP(false, true) : FP8Q_GROUP(false, false);
+        e = col ? FP8Q_GROUP(false, kColMajor) : FP8Q_GROUP(false, kRowMajor);
 #undef FP8Q_GROUP
     return launch_status(e);
 }
@@ -156,7 +162,7 @@ int fp8q_silu_and_mul_per_block_quant(const void *x, void *q, float *scales, int
                                       int32_t group_size, float eps, int32_t ue8m0,
                                       int32_t scale_layout, void *stream)
 {
-    int rc = check_common(x, q, scales, T, I, group_size, scale_layout);
+    int rc = check_common(x, q, scales, T, I, group_size, ue8m0, scale_layout);
     if (rc != FP8Q_OK)
         return rc;
     if (!valid_scale_eps(eps))
@@ -171,15 +177,18 @@ int fp8q_silu_and_mul_per_block_quant(const void *x, void *q, float *scales, int
     auto xp = static_cast<const uint16_t *>(x);
     auto qp = static_cast<uint8_t *>(q);
     const bool col = scale_layout == FP8Q_SCALES_COL_MAJOR;
+    const bool packed = scale_layout == FP8Q_SCALES_UE8M0_PACKED;
     const bool v8 = aligned(x, 32) && aligned(q, 32);
     cudaError_t e;
 #define FP8Q_SILU(U, C)                                                                          \
     (v8 ? launch_silu<U, C, true>(xp, qp, scales, n, G, T, I, eps, st)                          \
         : launch_silu<U, C, false>(xp, qp, scales, n, G, T, I, eps, st))
-    if (ue8m0)
-        e = col ? FP8Q_SILU(true, true) : FP8Q_SILU(true, false);
+    if (packed)
+        e = FP8Q_SILU(true, kPackedUe8m0);
+    else if (ue8m0)
+        e = col ? FP8Q_SILU(true, kColMajor) : FP8Q_SILU(true, kRowMajor);
     else
-        e = col ? FP8Q_SILU(false, true) : FP8Q_SILU(false, false);
+        e = col ? FP8Q_SILU(false, kColMajor) : FP8Q_SILU(false, kRowMajor);
 #undef FP8Q_SILU
     return launch_status(e);
 }
@@ -188,7 +197,7 @@ int fp8q_rms_norm_per_block_quant(const void *x, void *residual, const void *wei
                                   float *scales, int64_t T, int64_t H, int32_t group_size,
                                   float eps, int32_t ue8m0, int32_t scale_layout, void *stream)
 {
-    int rc = check_common(x, q, scales, T, H, group_size, scale_layout);
+    int rc = check_common(x, q, scales, T, H, group_size, ue8m0, scale_layout);
     if (rc != FP8Q_OK)
         return rc;
     if (!std::isfinite(eps) || eps < 0.0f)
@@ -210,15 +219,18 @@ int fp8q_rms_norm_per_block_quant(const void *x, void *residual, const void *wei
     auto wp = static_cast<const uint16_t *>(weight);
     auto qp = static_cast<uint8_t *>(q);
     const bool col = scale_layout == FP8Q_SCALES_COL_MAJOR;
+    const bool packed = scale_layout == FP8Q_SCALES_UE8M0_PACKED;
     const int t = int(T), h = int(H);
     cudaError_t e;
 #define FP8Q_RMS(U, C)                                                                           \
     (rp ? launch_rms<U, C, true>(xp, rp, wp, qp, scales, t, h, G, eps, st)                      \
         : launch_rms<U, C, false>(xp, rp, wp, qp, scales, t, h, G, eps, st))
-    if (ue8m0)
-        e = col ? FP8Q_RMS(true, true) : FP8Q_RMS(true, false);
+    if (packed)
+        e = FP8Q_RMS(true, kPackedUe8m0);
+    else if (ue8m0)
+        e = col ? FP8Q_RMS(true, kColMajor) : FP8Q_RMS(true, kRowMajor);
     else
-        e = col ? FP8Q_RMS(false, true) : FP8Q_RMS(false, false);
+        e = col ? FP8Q_RMS(false, kColMajor) : FP8Q_RMS(false, kRowMajor);
 #undef FP8Q_RMS
     return launch_status(e);
 }

@@ -190,6 +190,45 @@ __device__ __forceinline__ float quad_max(float m)
     return m;
 }
 
+// ------------------------------------------------------ scale layouts ---
+//
+// Where the scale of group g of token t goes (T tokens, G groups per row):
+//   kRowMajor     fp32 s[t*G + g]
+//   kColMajor     fp32 s[g*T + t]
+//   kPackedUe8m0  one byte per scale, its E8M0 exponent e (the scale is
+//                 2^(e - 127), UE8M0 only), four groups per 32-bit word:
+//                 word (g/4, t) at word index (g/4)*T_pad + t, byte g%4 of
+//                 it, T_pad = T rounded up to a multiple of 4.  The bytes of
+//                 groups past G and of tokens past T are written as 0 by the
+//                 threads of the last group and of the last token.
+constexpr int kRowMajor = 0, kColMajor = 1, kPackedUe8m0 = 2;
+
+template <int LAYOUT>
+__device__ __forceinline__ void store_scale(float *scales, float s, int64_t t, int64_t g, int64_t T, int64_t G)
+{
+    if (LAYOUT == kRowMajor) {
+        scales[t * G + g] = s;
+    } else if (LAYOUT == kColMajor) {
+        scales[g * T + t] = s;
+    } else {
+        uint8_t *b = reinterpret_cast<uint8_t *>(scales);
+        const int64_t T_pad = (T + 3) & ~int64_t(3), G_pad = (G + 3) & ~int64_t(3);
+        auto at = [&](int64_t gg, int64_t tt) -> uint8_t & { return b[((gg >> 2) * T_pad + tt) * 4 + (gg & 3)]; };
+        // a UE8M0 scale is a normal power of two: its exponent field is the byte
+        at(g, t) = uint8_t(__float_as_uint(s) >> 23);
+        if (t == T - 1)
+            for (int64_t tp = T; tp < T_pad; ++tp)
+                at(g, tp) = 0;
+        if (g == G - 1)
+            for (int64_t gp = G; gp < G_pad; ++gp) {
+                at(gp, t) = 0;
+                if (t == T - 1)
+                    for (int64_t tp = T; tp < T_pad; ++tp)
+                        at(gp, tp) = 0;
+            }
+    }
+}
+
 // ------------------------------------------------------------ scale -----
 
 // s = RN32(max(amax, eps) / 448); with UE8M0 the smallest power of two >= s.

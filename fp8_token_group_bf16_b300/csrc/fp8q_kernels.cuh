@@ -33,7 +33,7 @@ __device__ __forceinline__ void split_group(int64_t gi, int64_t G, int64_t &t, i
 // a warp read 8 adjacent groups (2 KiB) per pair of load instructions.
 // Out-of-range quads load a clamped, valid group and store nothing.
 // --------------------------------------------------------------------------
-template <bool UE8M0, bool COL, bool V8>
+template <bool UE8M0, int LAYOUT, bool V8>
 __global__ void __launch_bounds__(kCtaThreads) group_quant_kernel(const uint16_t *__restrict__ x,
                                                                   uint8_t *__restrict__ q,
                                                                   float *__restrict__ scales,
@@ -74,13 +74,9 @@ __global__ void __launch_bounds__(kCtaThreads) group_quant_kernel(const uint16_t
         if (gi < n_groups) {
             st32<V8>(q + gi * kGroup + sub * kValsPerLane, codes);
             if (sub == 0) {
-                if (COL) {
-                    int64_t t, g;
-                    split_group(gi, G, t, g);
-                    scales[g * T + t] = s;
-                } else {
-                    scales[gi] = s;
-                }
+                int64_t t, g;
+                split_group(gi, G, t, g);
+                store_scale<LAYOUT>(scales, s, t, g, T, G);
             }
         }
     }
@@ -127,7 +123,7 @@ __device__ __forceinline__ uint64_t silu_mul2(uint32_t aw, uint32_t bw)
     return f2_mul(q, b);
 }
 
-template <bool UE8M0, bool COL, bool V8>
+template <bool UE8M0, int LAYOUT, bool V8>
 __global__ void __launch_bounds__(kCtaThreads, 4) silu_quant_kernel(const uint16_t *__restrict__ x,
                                                                  uint8_t *__restrict__ q,
                                                                  float *__restrict__ scales,
@@ -165,7 +161,7 @@ __global__ void __launch_bounds__(kCtaThreads, 4) silu_quant_kernel(const uint16
     if (gi < n_groups) {
         st32<V8>(q + gi * kGroup + sub * kValsPerLane, codes);
         if (sub == 0)
-            scales[COL ? g * T + t : gi] = s;
+            store_scale<LAYOUT>(scales, s, t, g, T, G);
     }
 }
 

@@ -78,7 +78,7 @@ __device__ __forceinline__ float rms_inv(float hi, float lo, int H, float eps)
 // the same bytes).  Short-lived CTAs at ~64 registers leave room for six per
 // SM, whose loads overlap the others' arithmetic.
 
-template <int NG, bool UE8M0, bool COL, bool RES, bool V8>
+template <int NG, bool UE8M0, int LAYOUT, bool RES, bool V8>
 __global__ void __launch_bounds__(kRmsMaxThreads, NG == 1 ? 4 : (NG == 2 ? 2 : 1)) rms_row_kernel(
     const uint16_t *__restrict__ x, uint16_t *__restrict__ residual, const uint16_t *__restrict__ w,
     uint8_t *__restrict__ q, float *__restrict__ scales, int T, int H, int G, float eps)
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kRmsMaxThreads, NG == 1 ? 4 : (NG == 2 ? 2 : 1
         if (g < G) {
             st32<V8>(q + rbase + g * kGroup + sub * kValsPerLane, codes);
             if (sub == 0)
-                scales[COL ? int64_t(g) * T + row : int64_t(row) * G + g] = sc;
+                store_scale<LAYOUT>(scales, sc, row, g, T, G);
         }
     }
 }

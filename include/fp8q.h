@@ -29,7 +29,9 @@
  *  - `x`, `q`, `residual` and `weight` must be 16-byte aligned, `scales`
  *    4-byte aligned.  `q` must not alias `x`; `residual` must not alias `x`.
  *  - Scale layout: FP8Q_SCALES_ROW_MAJOR stores s[t*G + g];
- *    FP8Q_SCALES_COL_MAJOR stores s[g*T + t], G = H / group_size.
+ *    FP8Q_SCALES_COL_MAJOR stores s[g*T + t], G = H / group_size;
+ *    FP8Q_SCALES_UE8M0_PACKED stores exponent bytes (below).  A packed
+ *    layout without ue8m0 is FP8Q_ERR_INVALID_ARG.
  *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
  *    stream.  Calls only enqueue work and never synchronise, so they can be
  *    captured into CUDA graphs.
@@ -63,9 +65,23 @@ typedef enum {
 } fp8q_status;
 
 typedef enum {
-    FP8Q_SCALES_ROW_MAJOR = 0, /* s[t*G + g] */
-    FP8Q_SCALES_COL_MAJOR = 1  /* s[g*T + t] */
+    FP8Q_SCALES_ROW_MAJOR = 0,   /* fp32 s[t*G + g] */
+    FP8Q_SCALES_COL_MAJOR = 1,   /* fp32 s[g*T + t] */
+    FP8Q_SCALES_UE8M0_PACKED = 2 /* E8M0 exponent bytes, four groups per 32-bit word (below) */
 } fp8q_scale_layout;
+
+/*
+ * FP8Q_SCALES_UE8M0_PACKED (requires ue8m0 != 0): the power-of-two scales as
+ * the 8-bit exponents block-scaled FP8 GEMMs on Blackwell read, byte e
+ * standing for 2^(e - 127).  `scales` then addresses
+ * FP8Q_PACKED_SCALE_BYTES(T, G) bytes: 32-bit words, word (k, t) at word
+ * index k*T_pad + t (T_pad = T rounded up to a multiple of 4, k < ceil(G/4)),
+ * whose byte j (little-endian) is the exponent of group 4k + j of token t.
+ * Bytes of groups past G and of tokens past T are written as 0.  The pages
+ * name the "float32 ceiling E8M0" / UE8M0 scales but print no packed layout;
+ * this is the layout taken.
+ */
+#define FP8Q_PACKED_SCALE_BYTES(T, G) ((((G) + 3) / 4) * (((T) + 3) / 4 * 4) * 4)
 
 /* Longest rms_norm_per_block_quant row (H) the kernels accept (a row is held
  * in the registers of one CTA). */

@@ -27,6 +27,10 @@ def test_algorithmic_bytes_per_element():
     assert bench.algorithmic_bytes("rms_norm_per_block_quant", 256, 4096) == 3186688
     assert bench.algorithmic_bytes("rms_norm_per_block_quant", 256, 4096, True) == 7380992
     assert bench.algorithmic_bytes("silu_and_mul_per_block_quant", 1024, 12288) == 63307776
+    # packed UE8M0: one byte per group, groups padded to 4 and tokens to 4
+    assert bench.algorithmic_bytes("per_token_group_fp8_quant", 5, 768, packed=True) == 5 * 768 * 3 + 2 * 8 * 4
+    assert bench.algorithmic_bytes("silu_and_mul_per_block_quant", 4096, 25600, packed=True) == \
+        4096 * 25600 * 5 + 4096 * 200
     assert bench.step_bytes(1) == 21728 + 15520 + 10240 + 128800
 
 

@@ -77,10 +77,34 @@ def test_rejects_bad_shapes(lib):
     assert fq.fp8q_per_token_group_quant(A, Q, S, -1, 512, 128, 1e-10, 0, 0, None) == E
     assert fq.fp8q_per_token_group_quant(A, Q, S, 4, 0, 128, 1e-10, 0, 0, None) == E
     assert fq.fp8q_per_token_group_quant(A, Q, S, 4, 500, 128, 1e-10, 0, 0, None) == E
-    assert fq.fp8q_per_token_group_quant(A, Q, S, 4, 512, 128, 1e-10, 0, 2, None) == E
+    assert fq.fp8q_per_token_group_quant(A, Q, S, 4, 512, 128, 1e-10, 0, 3, None) == E
     assert fq.fp8q_per_token_group_quant(None, Q, S, 4, 512, 128, 1e-10, 0, 0, None) == E
     assert fq.fp8q_silu_and_mul_per_block_quant(A, Q, S, 4, 100, 128, 1e-10, 0, 0, None) == E
     assert fq.fp8q_rms_norm_per_block_quant(A, None, None, Q, S, 4, 512, 128, 1e-6, 0, 0, None) == E
+
+
+def test_packed_scales_need_ue8m0(lib):
+    """The packed layout holds exponent bytes, so it only takes power-of-two
+    scales: without ue8m0 every op refuses it before any CUDA call."""
+    E = fq.FP8Q_ERR_INVALID_ARG
+    P = fq.FP8Q_SCALES_UE8M0_PACKED
+    assert fq.fp8q_per_token_group_quant(A, Q, S, 4, 512, 128, 1e-10, 0, P, None) == E
+    assert fq.fp8q_silu_and_mul_per_block_quant(A, Q, S, 4, 512, 128, 1e-10, 0, P, None) == E
+    assert fq.fp8q_rms_norm_per_block_quant(A, None, A, Q, S, 4, 512, 128, 1e-6, 0, P, None) == E
+    # with ue8m0 it passes the checks: an empty input is then a no-op
+    assert fq.fp8q_per_token_group_quant(None, None, None, 0, 512, 128, 1e-10, 1, P, None) == 0
+
+
+def test_packed_scale_shape():
+    assert fq.packed_scale_shape(5, 6) == (2, 8)
+    assert fq.packed_scale_shape(4096, 56) == (14, 4096)
+    assert fq.packed_scale_shape(1, 1) == (1, 4)
+    # the header's byte count agrees with the binding's shape
+    text = open(HEADER).read()
+    assert "#define FP8Q_PACKED_SCALE_BYTES(T, G) ((((G) + 3) / 4) * (((T) + 3) / 4 * 4) * 4)" in text
+    for T, G in [(5, 6), (4096, 56), (1, 1), (7, 192)]:
+        k, tp = fq.packed_scale_shape(T, G)
+        assert k * tp * 4 == (((G) + 3) // 4) * (((T) + 3) // 4 * 4) * 4
 
 
 def test_rejects_bad_eps(lib):
