@@ -191,6 +191,42 @@ def silu_and_mul_per_block_quant(x_bits, group=128, eps=SCALE_EPS, ue8m0=False, 
     return q, s, sp
 
 
+# ------------------------------------------------------ per-token ops --
+# "Helion-Kernel in vLLM: PyTorch FP8 ohne CUDA", section "Welche Kernel
+# wurden in vLLM integriert": dynamic_per_token_scaled_fp8_quant,
+# rms_norm_dynamic_per_token_quant, silu_and_mul_dynamic_per_token_quant.
+# The same arithmetic as the per-group ops with the group spanning the row,
+# so each is the per-group function called with group = the row length; the
+# scales come back as [T] (one per token).
+
+
+def dynamic_per_token_scaled_fp8_quant(x_bits, eps=SCALE_EPS, ue8m0=False):
+    """x_bits uint16 [T,H] -> (q uint8 [T,H], scales [T], scales_pre [T])."""
+    x = _u16(x_bits)
+    q, s, sp = per_token_group_quant(x, group=x.shape[1], eps=eps, ue8m0=ue8m0)
+    return q, s[:, 0].copy(), sp[:, 0].copy()
+
+
+def rms_norm_dynamic_per_token_quant(x_bits, w_bits, residual_bits=None, eps=RMS_EPS, ue8m0=False,
+                                     want_values=False):
+    """Returns (q, scales [T], scales_pre [T], inv [T], residual_out or None),
+    plus the quantised fp32 values [T,H] when want_values."""
+    x = _u16(x_bits)
+    out = rms_norm_per_block_quant(x, w_bits, residual_bits, group=x.shape[1], eps=eps, ue8m0=ue8m0,
+                                   want_values=want_values)
+    q, s, sp = out[0], out[1][:, 0].copy(), out[2][:, 0].copy()
+    return (q, s, sp) + tuple(out[3:])
+
+
+def silu_and_mul_dynamic_per_token_quant(x_bits, eps=SCALE_EPS, ue8m0=False, want_values=False):
+    """x_bits uint16 [T, 2I] -> (q uint8 [T,I], scales [T], scales_pre [T]),
+    plus the quantised fp32 values [T,I] when want_values."""
+    x = _u16(x_bits)
+    out = silu_and_mul_per_block_quant(x, group=x.shape[1] // 2, eps=eps, ue8m0=ue8m0,
+                                       want_values=want_values)
+    return (out[0], out[1][:, 0].copy(), out[2][:, 0].copy()) + tuple(out[3:])
+
+
 def pack_ue8m0(scales_tg) -> np.ndarray:
     """Power-of-two scales [T, G] (fp32, row-major) -> the packed UE8M0 bytes
     (layout in fp8q_oracle.c), as a uint8 array [ceil(G/4), round_up(T, 4), 4]."""

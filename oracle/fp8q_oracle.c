@@ -43,6 +43,15 @@
  *          v = RN32( RN32( a / RN32(1 + expf(-a)) ) * b ),  then the group quant.
  *
  * Scale layouts: row-major s[t*G + g], column-major s[g*T + t], G = H/gs.
+ *
+ * Per-token variants.  "Helion-Kernel in vLLM: PyTorch FP8 ohne CUDA",
+ * section "Welche Kernel wurden in vLLM integriert", lists three per-token
+ * kernels next to the per-group ones: dynamic_per_token_scaled_fp8_quant,
+ * rms_norm_dynamic_per_token_quant and silu_and_mul_dynamic_per_token_quant.
+ * The pages give them no formula either; the plain reading is the same
+ * arithmetic with the group spanning the whole row (gs = H, or gs = I), i.e.
+ * one scale per token, s[t].  The functions below take any gs that divides
+ * the row, so the per-token ops are these functions called with gs = H.
  */
 #include "fp8q_oracle.h"
 
@@ -206,10 +215,10 @@ int oracle_per_token_group_quant(const uint16_t *x, uint8_t *q, float *scales, f
     int rc = check_shape(T, H, gs);
     if (rc)
         return rc;
-    if (gs > ORACLE_MAX_GROUP)
+    if (gs > ORACLE_MAX_ROW)
         return ORACLE_ERR_ARG;
     const int64_t G = H / gs;
-    float v[ORACLE_MAX_GROUP];
+    static float v[ORACLE_MAX_ROW];
     for (int64_t t = 0; t < T; ++t) {
         for (int64_t g = 0; g < G; ++g) {
             const uint16_t *xg = x + t * H + g * gs;
@@ -308,10 +317,10 @@ int oracle_silu_and_mul_per_block_quant(const uint16_t *x, uint8_t *q, float *sc
     int rc = check_shape(T, I, gs);
     if (rc)
         return rc;
-    if (gs > ORACLE_MAX_GROUP)
+    if (gs > ORACLE_MAX_ROW)
         return ORACLE_ERR_ARG;
     const int64_t G = I / gs;
-    float v[ORACLE_MAX_GROUP];
+    static float v[ORACLE_MAX_ROW];
     for (int64_t t = 0; t < T; ++t) {
         const uint16_t *xr = x + t * 2 * I;
         for (int64_t g = 0; g < G; ++g) {

@@ -10,6 +10,9 @@
  * `col_major` selects the scale layout: 0 -> s[t*G + g], 1 -> s[g*T + t].
  * `scales_pre` (may be NULL) receives each group's scale before the
  * power-of-two rounding (equal to `scales` when ue8m0 == 0).
+ * The group size gs may be anything that divides the row, up to
+ * ORACLE_MAX_ROW: gs = H gives the per-token variants (one scale per row).
+ * Not thread-safe (row buffers are static).
  */
 #ifndef FP8Q_ORACLE_H
 #define FP8Q_ORACLE_H
@@ -22,7 +25,6 @@ extern "C" {
 
 #define ORACLE_OK 0
 #define ORACLE_ERR_ARG 1
-#define ORACLE_MAX_GROUP 4096
 #define ORACLE_MAX_ROW (1 << 20)
 #define ORACLE_SCALE_EPS 1e-10f
 

@@ -427,9 +427,9 @@ def _exact_inv(ss: float, H: int, eps: float = RMS_EPS) -> float:
     return rn32(1 / Fraction(r))
 
 
-def _exact_op_b(xb, wb, rb, ue8m0):
+def _exact_op_b(xb, wb, rb, ue8m0, group: int = 128):
     T, H = xb.shape
-    G = H // 128
+    G = H // group
     q = np.zeros((T, H), np.uint8)
     s = np.zeros((T, G), np.float32)
     rout = None if rb is None else np.zeros_like(rb)
@@ -446,8 +446,8 @@ def _exact_op_b(xb, wb, rb, ue8m0):
         w = [bf16_to_float(int(b)) for b in wb]
         v = [rn32(Fraction(rn32(Fraction(zz) * Fraction(inv))) * Fraction(ww)) for zz, ww in zip(z, w)]
         for g in range(G):
-            codes, sc, _ = quant_group_exact(v[g * 128 : (g + 1) * 128], ue8m0)
-            q[t, g * 128 : (g + 1) * 128] = codes
+            codes, sc, _ = quant_group_exact(v[g * group : (g + 1) * group], ue8m0)
+            q[t, g * group : (g + 1) * group] = codes
             s[t, g] = sc
     return q, s, rout
 
@@ -627,6 +627,79 @@ def pin_silu_large_negative_gate():
     assert np.array_equal((q[0] >> 7).astype(bool), bneg)
 
 
+# ------------------------------------------------- per-token variants ----
+
+
+def pin_per_token_bruteforce():
+    """dynamic_per_token_scaled_fp8_quant on small inputs against the exact-
+    rational transcription with one group spanning the row."""
+    rs = np.random.default_rng(13)
+    xs = [inputs.bits(inputs.hand_rows(512))]
+    for scale in (1.0, 3e-3, 5e3):
+        f = torch.from_numpy((rs.standard_normal((2, 384)) * scale).astype(np.float32))
+        xs.append(inputs.bits(inputs.bf16(f)))
+    xs.append(inputs.bits(inputs.heavy_tailed_input(3, 256, seed=77)))
+    for xb in xs:
+        H = xb.shape[1]
+        for ue8m0 in (False, True):
+            q, s, _ = oracle.dynamic_per_token_scaled_fp8_quant(xb, ue8m0=ue8m0)
+            qe, se = _exact_op_a(xb, ue8m0, group=H)
+            assert s.shape == (xb.shape[0],) and np.array_equal(s, se[:, 0]), (ue8m0, s, se[:, 0])
+            assert np.array_equal(q, qe), (ue8m0, np.argwhere(q != qe)[:4])
+
+
+def pin_per_token_row_amax():
+    """One scale per row: the row's scale is the largest of its 128-groups'
+    scales (division by 448 is monotone), the row's largest |x| gets the
+    code +-448, and with UE8M0 the largest |code| of a row lies in [224, 448]."""
+    xb = inputs.bits(inputs.heavy_tailed_input(12, 7168, seed=inputs.SEED_SWEEP + 60))
+    for ue8m0 in (False, True):
+        q, s, sp = oracle.dynamic_per_token_scaled_fp8_quant(xb, ue8m0=ue8m0)
+        _, _, spg = oracle.per_token_group_quant(xb, ue8m0=ue8m0)
+        assert np.array_equal(sp, spg.max(axis=1))
+        xf = np.abs(bf16_bits_to_f32(xb))
+        top = q[np.arange(q.shape[0]), xf.argmax(axis=1)]
+        if ue8m0:
+            table = np.array([abs(float(e4m3_decode(c) or 0)) for c in range(256)])
+            full = table[q].max(axis=1)
+            assert np.all((full >= 224) & (full <= 448)), full
+        else:
+            assert np.all((top & 0x7F) == 0x7E), top
+
+
+def pin_rms_per_token_bruteforce():
+    x, w, r = inputs.rms_input(3, 256, seeds=(44, 45, 46))
+    xb, wb, rb = inputs.bits(x), inputs.bits(w), inputs.bits(r)
+    for res in (None, rb):
+        for ue8m0 in (False, True):
+            q, s, _, _, ro = oracle.rms_norm_dynamic_per_token_quant(xb, wb, res, ue8m0=ue8m0)
+            qe, se, re_ = _exact_op_b(xb, wb, res, ue8m0, group=256)
+            assert np.array_equal(s, se[:, 0]), (ue8m0, res is None)
+            assert np.array_equal(q, qe), (ue8m0, res is None, np.argwhere(q != qe)[:4])
+            if res is not None:
+                assert np.array_equal(ro, re_.astype(np.uint16))
+
+
+def pin_silu_per_token_bruteforce():
+    """silu_and_mul_dynamic_per_token_quant on a small input: codes within one
+    e4m3 step and the scale within 2e-6 of an exact transcription (the only
+    freedom is expf)."""
+    T, I = 2, 256
+    xb = inputs.bits(inputs.silu_input(T, I, seed=92))
+    for ue8m0 in (False, True):
+        q, s, sp = oracle.silu_and_mul_dynamic_per_token_quant(xb, ue8m0=ue8m0)
+        assert s.shape == (T,)
+        for t in range(T):
+            vals = [_silu_exact(bf16_to_float(int(xb[t, i])), bf16_to_float(int(xb[t, I + i])))[0]
+                    for i in range(I)]
+            codes, sc, pre = quant_group_exact(vals, ue8m0)
+            assert abs(float(sp[t]) - pre) <= 2e-6 * pre, t
+            if not ue8m0:
+                assert abs(float(s[t]) - sc) <= 2e-6 * sc
+            d = np.abs(ordinal(q[t]) - ordinal(np.array(codes, np.uint8)))
+            assert d.max() <= 1 and (d > 0).sum() <= 2, (t, d.max())
+
+
 ALL_PINS = [
     pin_golden_midpoints,
     pin_ue8m0_packed_golden,
@@ -648,6 +721,10 @@ ALL_PINS = [
     pin_rms_sumsq,
     pin_silu_values,
     pin_silu_bruteforce,
+    pin_per_token_bruteforce,
+    pin_per_token_row_amax,
+    pin_rms_per_token_bruteforce,
+    pin_silu_per_token_bruteforce,
     pin_e4m3_structured_exact,
     pin_ue8m0,
     pin_e4m3_torch_cast,

@@ -13,6 +13,10 @@ import oracle
 import pins
 
 MUTATIONS = {
+    "amax_over_first_128_values_only": (
+        "for (int64_t i = 0; i < gs; ++i) {\n        float a = fabsf(v[i]);",
+        "for (int64_t i = 0; i < (gs < 128 ? gs : 128); ++i) {\n        float a = fabsf(v[i]);",
+    ),
     "ties_away_from_zero": (
         "r = (fmodf(fl, 2.0f) == 0.0f) ? fl : fl + 1.0f;",
         "r = fl + 1.0f;",
