@@ -58,6 +58,13 @@ KERNEL_NAMES = {   # the kernel each op launches at the step's T
 # ------------------------------------------------------------------ bytes --
 
 
+PER_TOKEN_OPS = {
+    "dynamic_per_token_scaled_fp8_quant": "per_token_group_fp8_quant",
+    "rms_norm_dynamic_per_token_quant": "rms_norm_per_block_quant",
+    "silu_and_mul_dynamic_per_token_quant": "silu_and_mul_per_block_quant",
+}
+
+
 def algorithmic_bytes(op: str, T: int, H: int, residual: bool = False, packed: bool = False) -> int:
     """Bytes an op must move: each input read once, each output written once.
     group: x bf16 [T,H] in; e4m3 [T,H] and fp32 [T,H/128] out.
@@ -65,9 +72,12 @@ def algorithmic_bytes(op: str, T: int, H: int, residual: bool = False, packed: b
            residual [T,H] is read and written (+4 B per element).
     silu:  H is I; x bf16 [T,2I] in; e4m3 [T,I] and fp32 [T,I/128] out.
     packed: the scales are exponent bytes, [ceil(G/4), T rounded up to 4]
-           32-bit words, instead of fp32 [T, G]."""
+           32-bit words, instead of fp32 [T, G].
+    The per-token variants move the same bytes with one fp32 scale per row."""
     G = H // GROUP
     sb = -(-G // 4) * (-(-T // 4) * 4) * 4 if packed else 4 * T * G
+    if op in PER_TOKEN_OPS:
+        op, sb = PER_TOKEN_OPS[op], 4 * T
     if op == "per_token_group_fp8_quant":
         return T * H * 3 + sb
     if op == "rms_norm_per_block_quant":
@@ -604,6 +614,10 @@ def sweep(args):
         points.append(("per_token_group_fp8_quant", T, A_H, True, "packed", False))
         points.append(("rms_norm_per_block_quant", T, B_H, True, "packed", False))
         points.append(("silu_and_mul_per_block_quant", T, C_I, True, "packed", False))
+    for T in (64, 512, 4096, 16384):   # per-token variants, one scale per row
+        points.append(("dynamic_per_token_scaled_fp8_quant", T, A_H, False, "token", False))
+        points.append(("rms_norm_dynamic_per_token_quant", T, B_H, False, "token", False))
+        points.append(("silu_and_mul_dynamic_per_token_quant", T, C_I, False, "token", False))
     rows = []
     for op, T, H, ue8m0, lay, res in points:
         nbytes = algorithmic_bytes(op, T, H, res, packed=lay == "packed")
@@ -612,6 +626,14 @@ def sweep(args):
         def make(op=op, T=T, H=H, ue8m0=ue8m0, lay=lay, res=res, G=G):
             xin = torch.randn(T, 2 * H if op.startswith("silu") else H, device=dev).to(torch.bfloat16)
             q = torch.empty(T, H, dtype=e4, device=dev)
+            if lay == "token":
+                s = torch.empty(T, 1, device=dev)
+                if op == "dynamic_per_token_scaled_fp8_quant":
+                    return lambda: fq.dynamic_per_token_scaled_fp8_quant(xin, ue8m0=ue8m0, q=q, scales=s)
+                if op == "silu_and_mul_dynamic_per_token_quant":
+                    return lambda: fq.silu_and_mul_dynamic_per_token_quant(xin, ue8m0=ue8m0, q=q, scales=s)
+                w = torch.randn(H, device=dev).to(torch.bfloat16)
+                return lambda: fq.rms_norm_dynamic_per_token_quant(xin, w, None, ue8m0=ue8m0, q=q, scales=s)
             if lay == "packed":
                 s = torch.empty(fq.packed_scale_shape(T, G), dtype=torch.int32, device=dev)
             else:

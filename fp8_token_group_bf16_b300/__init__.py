@@ -4,11 +4,16 @@ The compute lives in ``libfp8q.so`` (hand-written CUDA for sm_103a, C ABI in
 ``include/fp8q.h``).  This package is a thin ctypes binding over it:
 
 * ``fp8q_per_token_group_quant``, ``fp8q_rms_norm_per_block_quant``,
-  ``fp8q_silu_and_mul_per_block_quant``, ``fp8q_f32_to_e4m3``,
+  ``fp8q_silu_and_mul_per_block_quant``, their per-token variants
+  ``fp8q_dynamic_per_token_scaled_fp8_quant``,
+  ``fp8q_rms_norm_dynamic_per_token_quant``,
+  ``fp8q_silu_and_mul_dynamic_per_token_quant``, and ``fp8q_f32_to_e4m3``,
   ``fp8q_status_string`` -- the C entry points under their own names, taking
   raw device pointers (ints) and sizes, returning the status code;
 * ``per_token_group_fp8_quant``, ``rms_norm_per_block_quant``,
-  ``silu_and_mul_per_block_quant`` -- the same calls on torch tensors:
+  ``silu_and_mul_per_block_quant``, ``dynamic_per_token_scaled_fp8_quant``,
+  ``rms_norm_dynamic_per_token_quant``,
+  ``silu_and_mul_dynamic_per_token_quant`` -- the same calls on torch tensors:
   argument checks, output allocation, the current CUDA stream, and an
   exception on a non-zero status.  Every step of the computation runs in the
   library's kernels; there is no CPU fallback.  If the library is missing or
@@ -34,12 +39,16 @@ FP8Q_SCALES_ROW_MAJOR = 0
 FP8Q_SCALES_COL_MAJOR = 1
 FP8Q_SCALES_UE8M0_PACKED = 2
 FP8Q_RMS_MAX_H = 32768
+FP8Q_TOKEN_MAX_COLS = 65536
 GROUP = 128
 
 EXPORTS = (
     "fp8q_per_token_group_quant",
     "fp8q_rms_norm_per_block_quant",
     "fp8q_silu_and_mul_per_block_quant",
+    "fp8q_dynamic_per_token_scaled_fp8_quant",
+    "fp8q_rms_norm_dynamic_per_token_quant",
+    "fp8q_silu_and_mul_dynamic_per_token_quant",
     "fp8q_f32_to_e4m3",
     "fp8q_status_string",
     "fp8q_version",
@@ -68,8 +77,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.fp8q_per_token_group_quant.argtypes = [P, P, P, I64, I64, I32, F, I32, I32, P]
     L.fp8q_rms_norm_per_block_quant.argtypes = [P, P, P, P, P, I64, I64, I32, F, I32, I32, P]
     L.fp8q_silu_and_mul_per_block_quant.argtypes = [P, P, P, I64, I64, I32, F, I32, I32, P]
+    L.fp8q_dynamic_per_token_scaled_fp8_quant.argtypes = [P, P, P, I64, I64, F, I32, P]
+    L.fp8q_rms_norm_dynamic_per_token_quant.argtypes = [P, P, P, P, P, I64, I64, F, I32, P]
+    L.fp8q_silu_and_mul_dynamic_per_token_quant.argtypes = [P, P, P, I64, I64, F, I32, P]
     L.fp8q_f32_to_e4m3.argtypes = [P, P, I64, P]
-    for n in EXPORTS[:4]:
+    for n in EXPORTS[:7]:
         getattr(L, n).restype = ctypes.c_int
     L.fp8q_status_string.argtypes = [ctypes.c_int]
     L.fp8q_status_string.restype = ctypes.c_char_p
@@ -97,6 +109,19 @@ def fp8q_silu_and_mul_per_block_quant(x, q, scales, T, I, group_size, eps, ue8m0
                                       stream):
     return load().fp8q_silu_and_mul_per_block_quant(x, q, scales, T, I, group_size, eps, ue8m0,
                                                     scale_layout, stream)
+
+
+def fp8q_dynamic_per_token_scaled_fp8_quant(x, q, scales, T, H, eps, ue8m0, stream):
+    return load().fp8q_dynamic_per_token_scaled_fp8_quant(x, q, scales, T, H, eps, ue8m0, stream)
+
+
+def fp8q_rms_norm_dynamic_per_token_quant(x, residual, weight, q, scales, T, H, eps, ue8m0, stream):
+    return load().fp8q_rms_norm_dynamic_per_token_quant(x, residual, weight, q, scales, T, H, eps, ue8m0,
+                                                        stream)
+
+
+def fp8q_silu_and_mul_dynamic_per_token_quant(x, q, scales, T, I, eps, ue8m0, stream):
+    return load().fp8q_silu_and_mul_dynamic_per_token_quant(x, q, scales, T, I, eps, ue8m0, stream)
 
 
 def fp8q_f32_to_e4m3(v, out, n, stream):
@@ -242,6 +267,70 @@ def silu_and_mul_per_block_quant(x, group_size: int = GROUP, eps: float = 1e-10,
     _check(fp8q_silu_and_mul_per_block_quant(
         x.data_ptr(), q.data_ptr(), sp, T, I, group_size, eps, int(ue8m0), layout,
         _stream_ptr(x, stream)), "silu_and_mul_per_block_quant")
+    return q, scales
+
+
+# ------------------------------------------------- per-token variants ----
+
+
+def _token_outputs(x, T, cols, q, scales):
+    torch = _torch()
+    if q is None:
+        q = torch.empty((T, cols), dtype=torch.float8_e4m3fn, device=x.device)
+    if scales is None:
+        scales = torch.empty((T, 1), dtype=torch.float32, device=x.device)
+    if scales.numel() != T or scales.dtype != torch.float32 or not scales.is_contiguous():
+        raise ValueError(f"per-token scales must be a contiguous fp32 tensor of {T} elements")
+    return q, scales
+
+
+def dynamic_per_token_scaled_fp8_quant(x, eps: float = 1e-10, ue8m0: bool = False, q=None, scales=None,
+                                       stream=None):
+    """x bf16 [T, H] -> (q float8_e4m3fn [T, H], scales fp32 [T, 1]): one scale per token."""
+    _need_cuda_bf16("x", x)
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D [T, H]")
+    T, H = x.shape
+    q, scales = _token_outputs(x, T, H, q, scales)
+    _check(fp8q_dynamic_per_token_scaled_fp8_quant(x.data_ptr(), q.data_ptr(), scales.data_ptr(), T, H, eps,
+                                                   int(ue8m0), _stream_ptr(x, stream)),
+           "dynamic_per_token_scaled_fp8_quant")
+    return q, scales
+
+
+def rms_norm_dynamic_per_token_quant(x, weight, residual=None, eps: float = 1e-6, ue8m0: bool = False, q=None,
+                                     scales=None, stream=None):
+    """RMSNorm(x [+ residual]) * weight, then one FP8 scale per token.
+
+    ``residual`` (optional) is updated in place to bf16(x + residual), as in
+    rms_norm_per_block_quant.  Returns (q [T, H], scales [T, 1])."""
+    _need_cuda_bf16("x", x)
+    _need_cuda_bf16("weight", weight)
+    if residual is not None:
+        _need_cuda_bf16("residual", residual)
+        if residual.shape != x.shape:
+            raise ValueError("residual must have the shape of x")
+    if x.dim() != 2 or weight.dim() != 1 or weight.shape[0] != x.shape[1]:
+        raise ValueError("x must be [T, H] and weight [H]")
+    T, H = x.shape
+    q, scales = _token_outputs(x, T, H, q, scales)
+    _check(fp8q_rms_norm_dynamic_per_token_quant(
+        x.data_ptr(), residual.data_ptr() if residual is not None else None, weight.data_ptr(), q.data_ptr(),
+        scales.data_ptr(), T, H, eps, int(ue8m0), _stream_ptr(x, stream)), "rms_norm_dynamic_per_token_quant")
+    return q, scales
+
+
+def silu_and_mul_dynamic_per_token_quant(x, eps: float = 1e-10, ue8m0: bool = False, q=None, scales=None,
+                                         stream=None):
+    """x bf16 [T, 2I] = [gate | up] -> (q [T, I], scales [T, 1]) of silu(gate) * up."""
+    _need_cuda_bf16("x", x)
+    if x.dim() != 2 or x.shape[1] % 2:
+        raise ValueError("x must be [T, 2I]")
+    T, I = x.shape[0], x.shape[1] // 2
+    q, scales = _token_outputs(x, T, I, q, scales)
+    _check(fp8q_silu_and_mul_dynamic_per_token_quant(x.data_ptr(), q.data_ptr(), scales.data_ptr(), T, I, eps,
+                                                     int(ue8m0), _stream_ptr(x, stream)),
+           "silu_and_mul_dynamic_per_token_quant")
     return q, scales
 
 

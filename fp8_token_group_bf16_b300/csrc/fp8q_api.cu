@@ -3,6 +3,7 @@
 #include "fp8q.h"
 #include "fp8q_kernels.cuh"
 #include "fp8q_rms.cuh"
+#include "fp8q_token.cuh"
 
 #include <cmath>
 #include <cstdint>
@@ -11,6 +12,8 @@
 namespace {
 
 using namespace fp8q;
+
+static_assert(FP8Q_TOKEN_MAX_COLS == kTokenMaxGroups * kGroup, "per-token row limit");
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -55,23 +58,41 @@ int launch_status(cudaError_t launched)
 
 // Launch with programmatic stream serialization allowed: the kernel may be
 // scheduled while its predecessor on the stream drains, and waits for it
-// (griddepcontrol.wait) before touching global memory.
+// (griddepcontrol.wait) before touching global memory.  cluster > 1 groups
+// the CTAs into thread-block clusters of that many along x; smem is the
+// dynamic shared memory per CTA.
 template <typename... KArgs, typename... Args>
-cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t st, Args... args)
+cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, unsigned cluster, size_t smem,
+                      cudaStream_t st, Args... args)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
 #ifndef FP8Q_NO_PDL
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
 #endif
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = n ? attr : nullptr;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t st, Args... args)
+{
+    return launch_ex(kernel, grid, block, 1u, 0, st, args...);
 }
 
 template <bool U, int C, bool V>
@@ -117,6 +138,86 @@ cudaError_t launch_rms(const uint16_t *x, uint16_t *res, const uint16_t *w, uint
         return FP8Q_ROW(2);
     return FP8Q_ROW(4);
 #undef FP8Q_ROW
+}
+
+// Per-token ops A and C: C CTAs per row (a cluster when C > 1), gpc =
+// ceil(G / C) groups per CTA, one quad per group.  C is the smallest count
+// from ceil(G / 64) to 8 whose CTAs leave the fewest idle lanes (200 groups:
+// 5 CTAs of 40 quads rather than 4 of 50 quads in 56-quad blocks).
+int token_ctas_per_row(int G)
+{
+    int best = (G + kGroupsPerCta - 1) / kGroupsPerCta, best_idle = 1 << 30;
+    for (int C = best; C <= kTokenMaxCluster; ++C) {
+        const int gpc = (G + C - 1) / C;
+        if ((C - 1) * gpc >= G)
+            continue;   // the last CTA would own no group
+        const int idle = C * ((gpc * kLanesPerGroup + 31) / 32) * 32 - G * kLanesPerGroup;
+        if (idle < best_idle) {
+            best = C;
+            best_idle = idle;
+        }
+    }
+    return best;
+}
+
+template <bool SILU>
+int launch_token(const uint16_t *x, uint8_t *q, float *s, int64_t T, int64_t cols, float eps, bool ue8m0,
+                 cudaStream_t st)
+{
+    const int G = int(cols / kGroup);
+    const int C = token_ctas_per_row(G);
+    const int gpc = (G + C - 1) / C;
+    if (C > kTokenMaxCluster || (C - 1) * gpc >= G || T * C >= (int64_t(1) << 31))
+        return FP8Q_ERR_UNSUPPORTED;
+    const int threads = ((gpc * kLanesPerGroup + 31) / 32) * 32;
+    const bool v8 = aligned(x, 32) && aligned(q, 32);
+    const dim3 grid{unsigned(T * C)}, block{unsigned(threads)};
+    const int c = int(cols);
+    cudaError_t e;
+#define FP8Q_TOKEN(U, V)                                                                         \
+    launch_ex(SILU ? token_silu_kernel<U, V> : token_quant_kernel<U, V>, grid, block, unsigned(C), 0, st, x, q, s, \
+              c, G, gpc, C, eps)
+    if (ue8m0)
+        e = v8 ? FP8Q_TOKEN(true, true) : FP8Q_TOKEN(true, false);
+    else
+        e = v8 ? FP8Q_TOKEN(false, true) : FP8Q_TOKEN(false, false);
+#undef FP8Q_TOKEN
+    return launch_status(e);
+}
+
+// Checks shared by the per-token entry points (ops A and C): the row is a
+// whole number of 128-value chunks, at most 512 of them.
+int check_token(const void *x, const void *q, const float *scales, int64_t T, int64_t cols, float eps)
+{
+    if (T < 0 || cols <= 0 || !valid_scale_eps(eps))
+        return FP8Q_ERR_INVALID_ARG;
+    if (cols % kGroup != 0 || cols > int64_t(kTokenMaxGroups) * kGroup)
+        return FP8Q_ERR_UNSUPPORTED;
+    if (T == 0)
+        return FP8Q_OK;
+    if (!x || !q || !scales)
+        return FP8Q_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(q, 16) || !aligned(scales, 4))
+        return FP8Q_ERR_MISALIGNED;
+    return FP8Q_OK;
+}
+
+// Checks shared by the two RMSNorm entry points (after the scale checks).
+int check_rms(const void *residual, const void *weight, int64_t T, int64_t H, float eps)
+{
+    if (!std::isfinite(eps) || eps < 0.0f)
+        return FP8Q_ERR_INVALID_ARG;
+    if (H > FP8Q_RMS_MAX_H)
+        return FP8Q_ERR_UNSUPPORTED;
+    if (T == 0)
+        return FP8Q_OK;
+    if (!weight)
+        return FP8Q_ERR_INVALID_ARG;
+    if (!aligned(weight, 16) || (residual && !aligned(residual, 16)))
+        return FP8Q_ERR_MISALIGNED;
+    if (T >= (int64_t(1) << 30))
+        return FP8Q_ERR_UNSUPPORTED;
+    return FP8Q_OK;
 }
 
 }  // namespace
@@ -200,18 +301,8 @@ int fp8q_rms_norm_per_block_quant(const void *x, void *residual, const void *wei
     int rc = check_common(x, q, scales, T, H, group_size, ue8m0, scale_layout);
     if (rc != FP8Q_OK)
         return rc;
-    if (!std::isfinite(eps) || eps < 0.0f)
-        return FP8Q_ERR_INVALID_ARG;
-    if (H > FP8Q_RMS_MAX_H)
-        return FP8Q_ERR_UNSUPPORTED;
-    if (T == 0)
-        return FP8Q_OK;
-    if (!weight)
-        return FP8Q_ERR_INVALID_ARG;
-    if (!aligned(weight, 16) || (residual && !aligned(residual, 16)))
-        return FP8Q_ERR_MISALIGNED;
-    if (T >= (int64_t(1) << 30))
-        return FP8Q_ERR_UNSUPPORTED;
+    if ((rc = check_rms(residual, weight, T, H, eps)) != FP8Q_OK || T == 0)
+        return rc;
     const int G = int(H / kGroup);
     auto st = static_cast<cudaStream_t>(stream);
     auto xp = static_cast<const uint16_t *>(x);
@@ -231,6 +322,56 @@ int fp8q_rms_norm_per_block_quant(const void *x, void *residual, const void *wei
         e = col ? FP8Q_RMS(true, kColMajor) : FP8Q_RMS(true, kRowMajor);
     else
         e = col ? FP8Q_RMS(false, kColMajor) : FP8Q_RMS(false, kRowMajor);
+#undef FP8Q_RMS
+    return launch_status(e);
+}
+
+int fp8q_dynamic_per_token_scaled_fp8_quant(const void *x, void *q, float *scales, int64_t T, int64_t H,
+                                            float eps, int32_t ue8m0, void *stream)
+{
+    const int rc = check_token(x, q, scales, T, H, eps);
+    if (rc != FP8Q_OK || T == 0)
+        return rc;
+    return launch_token<false>(static_cast<const uint16_t *>(x), static_cast<uint8_t *>(q), scales, T, H,
+                               eps, ue8m0 != 0, static_cast<cudaStream_t>(stream));
+}
+
+int fp8q_silu_and_mul_dynamic_per_token_quant(const void *x, void *q, float *scales, int64_t T, int64_t I,
+                                              float eps, int32_t ue8m0, void *stream)
+{
+    const int rc = check_token(x, q, scales, T, I, eps);
+    if (rc != FP8Q_OK || T == 0)
+        return rc;
+    return launch_token<true>(static_cast<const uint16_t *>(x), static_cast<uint8_t *>(q), scales, T, I,
+                              eps, ue8m0 != 0, static_cast<cudaStream_t>(stream));
+}
+
+int fp8q_rms_norm_dynamic_per_token_quant(const void *x, void *residual, const void *weight, void *q,
+                                          float *scales, int64_t T, int64_t H, float eps, int32_t ue8m0,
+                                          void *stream)
+{
+    if (T < 0 || H <= 0)
+        return FP8Q_ERR_INVALID_ARG;
+    if (H % kGroup != 0)
+        return FP8Q_ERR_UNSUPPORTED;
+    int rc = check_rms(residual, weight, T, H, eps);
+    if (rc != FP8Q_OK || T == 0)
+        return rc;
+    if (!x || !q || !scales)
+        return FP8Q_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(q, 16) || !aligned(scales, 4))
+        return FP8Q_ERR_MISALIGNED;
+    auto st = static_cast<cudaStream_t>(stream);
+    auto xp = static_cast<const uint16_t *>(x);
+    auto rp = static_cast<uint16_t *>(residual);
+    auto wp = static_cast<const uint16_t *>(weight);
+    auto qp = static_cast<uint8_t *>(q);
+    const int t = int(T), h = int(H), G = int(H / kGroup);
+    cudaError_t e;
+#define FP8Q_RMS(U)                                                                              \
+    (rp ? launch_rms<U, kPerToken, true>(xp, rp, wp, qp, scales, t, h, G, eps, st)              \
+        : launch_rms<U, kPerToken, false>(xp, rp, wp, qp, scales, t, h, G, eps, st))
+    e = ue8m0 ? FP8Q_RMS(true) : FP8Q_RMS(false);
 #undef FP8Q_RMS
     return launch_status(e);
 }
@@ -265,7 +406,7 @@ const char *fp8q_status_string(int status)
     }
 }
 
-int fp8q_version(void) { return 400; }
+int fp8q_version(void) { return 500; }
 
 
 }  // extern "C"

@@ -201,7 +201,10 @@ __device__ __forceinline__ float quad_max(float m)
 //                 it, T_pad = T rounded up to a multiple of 4.  The bytes of
 //                 groups past G and of tokens past T are written as 0 by the
 //                 threads of the last group and of the last token.
-constexpr int kRowMajor = 0, kColMajor = 1, kPackedUe8m0 = 2;
+//   kPerToken     one fp32 scale per token, s[t]; the kernels that use it
+//                 take the maximum over the whole row and store it
+//                 themselves, not through store_scale.
+constexpr int kRowMajor = 0, kColMajor = 1, kPackedUe8m0 = 2, kPerToken = 3;
 
 template <int LAYOUT>
 __device__ __forceinline__ void store_scale(float *scales, float s, int64_t t, int64_t g, int64_t T, int64_t G)

@@ -77,6 +77,12 @@ __device__ __forceinline__ float rms_inv(float hi, float lo, int H, float eps)
 // joins the warps.  The weight is read through L1 (every CTA of a SM reads
 // the same bytes).  Short-lived CTAs at ~64 registers leave room for six per
 // SM, whose loads overlap the others' arithmetic.
+//
+// LAYOUT == kPerToken is rms_norm_dynamic_per_token_quant: one scale for the
+// whole row.  The normalised values are then formed twice from the registers
+// (once for the row maximum, joined across warps by a second barrier, once to
+// quantise), which is two multiplies per pair of values instead of keeping
+// another 32 registers per group alive.
 
 template <int NG, bool UE8M0, int LAYOUT, bool RES, bool V8>
 __global__ void __launch_bounds__(kRmsMaxThreads, NG == 1 ? 4 : (NG == 2 ? 2 : 1)) rms_row_kernel(
@@ -84,6 +90,7 @@ __global__ void __launch_bounds__(kRmsMaxThreads, NG == 1 ? 4 : (NG == 2 ? 2 : 1
     uint8_t *__restrict__ q, float *__restrict__ scales, int T, int H, int G, float eps)
 {
     __shared__ float2 red[kRmsMaxThreads / 32];
+    __shared__ float redm[kRmsMaxThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, sub = tid & 3, quad = tid >> 2, warp = tid >> 5;
     const int nq = blockDim.x >> 2, nwarps = blockDim.x >> 5;
     const int row = blockIdx.x;
@@ -137,33 +144,81 @@ __global__ void __launch_bounds__(kRmsMaxThreads, NG == 1 ? 4 : (NG == 2 ? 2 : 1
     const float inv = rms_inv(a.x, a.y, H, eps);
     const uint64_t inv2 = f2_pack(inv, inv);
 
-    // ---- pass 2: v = (z * inv) * w, group scale, codes
-#pragma unroll
-    for (int j = 0; j < NG; ++j) {
-        const int g = quad + nq * j;
-        uint64_t v[4][4];
+    if constexpr (LAYOUT == kPerToken) {
+        // ---- pass 2: row maximum of v = (z * inv) * w
         float mm[2] = {0.0f, 0.0f};
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int j = 0; j < NG; ++j) {
+            if (quad + nq * j < G) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int k = 4 * i + e;
-                v[i][e] = f2_mul(f2_mul(f2_from_bf16x2(z[j][k]), inv2), f2_from_bf16x2(wr[j][k]));
-                float va, vb;
-                f2_unpack(v[i][e], va, vb);
-                mm[e & 1] = absmax3(mm[e & 1], va, vb);
+                for (int k = 0; k < 16; ++k) {
+                    float va, vb;
+                    f2_unpack(f2_mul(f2_mul(f2_from_bf16x2(z[j][k]), inv2), f2_from_bf16x2(wr[j][k])), va, vb);
+                    mm[k & 1] = absmax3(mm[k & 1], va, vb);
+                }
             }
-        const float amax = quad_max(fmaxf(mm[0], mm[1]));
+        }
+        float m = fmaxf(mm[0], mm[1]);
+#pragma unroll
+        for (int o = 1; o <= 16; o <<= 1)
+            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        if (lane == 0)
+            redm[warp] = m;
+        __syncthreads();
+        float amax = redm[0];
+        for (int i = 1; i < nwarps; ++i)
+            amax = fmaxf(amax, redm[i]);
         const float sc = group_scale<UE8M0>(amax, kScaleFloor);
         const float rc = scale_recip<UE8M0>(sc);
-        uint32_t codes[8];
+
+        // ---- pass 3: the same values again, codes
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            quant8<UE8M0>(v[i], sc, rc, codes[2 * i], codes[2 * i + 1]);
-        if (g < G) {
-            st32<V8>(q + rbase + g * kGroup + sub * kValsPerLane, codes);
-            if (sub == 0)
-                store_scale<LAYOUT>(scales, sc, row, g, T, G);
+        for (int j = 0; j < NG; ++j) {
+            const int g = quad + nq * j;
+            uint64_t v[4][4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    v[i][e] = f2_mul(f2_mul(f2_from_bf16x2(z[j][4 * i + e]), inv2), f2_from_bf16x2(wr[j][4 * i + e]));
+            uint32_t codes[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                quant8<UE8M0>(v[i], sc, rc, codes[2 * i], codes[2 * i + 1]);
+            if (g < G)
+                st32<V8>(q + rbase + g * kGroup + sub * kValsPerLane, codes);
+        }
+        if (tid == 0)
+            scales[row] = sc;
+    } else {
+        // ---- pass 2: v = (z * inv) * w, group scale, codes
+#pragma unroll
+        for (int j = 0; j < NG; ++j) {
+            const int g = quad + nq * j;
+            uint64_t v[4][4];
+            float mm[2] = {0.0f, 0.0f};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int k = 4 * i + e;
+                    v[i][e] = f2_mul(f2_mul(f2_from_bf16x2(z[j][k]), inv2), f2_from_bf16x2(wr[j][k]));
+                    float va, vb;
+                    f2_unpack(v[i][e], va, vb);
+                    mm[e & 1] = absmax3(mm[e & 1], va, vb);
+                }
+            const float amax = quad_max(fmaxf(mm[0], mm[1]));
+            const float sc = group_scale<UE8M0>(amax, kScaleFloor);
+            const float rc = scale_recip<UE8M0>(sc);
+            uint32_t codes[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                quant8<UE8M0>(v[i], sc, rc, codes[2 * i], codes[2 * i + 1]);
+            if (g < G) {
+                st32<V8>(q + rbase + g * kGroup + sub * kValsPerLane, codes);
+                if (sub == 0)
+                    store_scale<LAYOUT>(scales, sc, row, g, T, G);
+            }
         }
     }
 }

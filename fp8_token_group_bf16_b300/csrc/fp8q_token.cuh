@@ -1,0 +1,188 @@
+// Per-token ("dynamic per-token") quantisation for sm_103a: one scale per
+// token row instead of one per 128-group.  dynamic_per_token_scaled_fp8_quant
+// is token_quant_kernel, silu_and_mul_dynamic_per_token_quant is
+// token_silu_kernel; the RMSNorm variant is rms_row_kernel with the
+// kPerToken scale layout.
+//
+// The row-wide amax is the only step the per-group kernels do not have.  A
+// row of up to 64 groups (8192 values) is one CTA of quads, as in the group
+// kernels, each lane holding 32 values.  A longer row is
+// split over a thread-block cluster of C <= 8 CTAs (one per 64 groups or
+// fewer), and the CTAs exchange their partial maxima through distributed
+// shared memory: each warp's maximum is written straight into the matching
+// slot of every CTA of the cluster, one cluster barrier later every CTA reads
+// all C x nwarps partials from its own shared memory.  Nothing is re-read
+// from HBM and no second kernel is needed.
+#pragma once
+
+#include "fp8q_kernels.cuh"
+
+namespace fp8q {
+
+constexpr int kTokenMaxCluster = 8;                        // portable cluster size
+constexpr int kTokenMaxWarps = kCtaThreads / 32;           // 8
+constexpr int kTokenMaxGroups = kTokenMaxCluster * kGroupsPerCta;   // 512 groups = 65536 values
+
+// Cluster barrier halves.  Every thread of every CTA of the cluster executes
+// each of them exactly once, in uniform control flow (like __syncthreads), so
+// no barrier can wait on a thread that never arrives.
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive_release()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_acquire()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Store v at the address of `local` in the shared memory of CTA `rank` of
+// this cluster.
+__device__ __forceinline__ void st_cluster_f32(float *local, uint32_t rank, float v)
+{
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(a), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+
+// The row maximum from each warp's maximum m: every CTA of the row's cluster
+// (C of them, rank `rank`; C = 1 is a single CTA) ends with the maximum over
+// the whole row.  `part` is this CTA's slot array [kTokenMaxCluster][kTokenMaxWarps].
+// With C > 1 the caller has executed cluster_arrive_relaxed() once at the
+// start of the kernel; the wait here pairs with it, so that every CTA of the
+// cluster is known to be running before its shared memory is written.
+__device__ __forceinline__ float row_max_exchange(float m, float *part, int rank, int C)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+#pragma unroll
+    for (int o = 1; o <= 16; o <<= 1)
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (C == 1) {
+        if (lane == 0)
+            part[warp] = m;
+        __syncthreads();
+    } else {
+        cluster_wait_acquire();
+        if (lane < C)
+            st_cluster_f32(&part[rank * kTokenMaxWarps + warp], uint32_t(lane), m);
+        __syncwarp();
+        cluster_arrive_release();
+        cluster_wait_acquire();   // all partials have landed; no remote access follows
+    }
+    float amax = 0.0f;
+    for (int r = 0; r < C; ++r)
+        for (int w = 0; w < nwarps; ++w)
+            amax = fmaxf(amax, part[r * kTokenMaxWarps + w]);
+    return amax;
+}
+
+// Launch shape of both per-token kernels: grid = T * C CTAs, clusters of C
+// along x (C = 1: an ordinary launch); CTA rank r of row t owns groups
+// [r * gpc, min((r + 1) * gpc, G)) with one quad per group.  cols is the
+// output row length.  Inactive quads read their CTA's first group,
+// contribute 0 to the maximum and store nothing.
+
+// dynamic_per_token_scaled_fp8_quant.  Only the 16 raw bf16x2 words of a
+// lane stay live across the row exchange (the maximum of |x| is taken on the
+// bf16 values, which is exact); the fp32 values are formed afterwards, as in
+// the per-group kernel, which keeps the register count at the per-group
+// kernel's.
+template <bool UE8M0, bool V8>
+__global__ void __launch_bounds__(kCtaThreads, 5) token_quant_kernel(const uint16_t *__restrict__ x,
+                                                                   uint8_t *__restrict__ q,
+                                                                   float *__restrict__ scales, int cols,
+                                                                   int G, int gpc, int C, float eps)
+{
+    __shared__ float part[kTokenMaxCluster * kTokenMaxWarps];
+    const int tid = threadIdx.x, sub = tid & 3, quad = tid >> 2;
+    const int row = blockIdx.x / C, rank = blockIdx.x - row * C;
+    const int g0 = rank * gpc, g = g0 + quad;
+    const bool act = quad < gpc && g < G;
+    const int64_t off = int64_t(row) * cols + int64_t(act ? g : g0) * kGroup + sub * kValsPerLane;
+
+    if (C > 1)
+        cluster_arrive_relaxed();
+    wait_for_producer();
+    allow_consumer_launch();
+
+    uint32_t raw[16];
+    ld64_stream<V8>(x + off, raw);
+    float m = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+        m = absmax3(m, bf_lo(raw[k]), bf_hi(raw[k]));
+    const float amax = row_max_exchange(act ? m : 0.0f, part, rank, C);
+
+    const float s = group_scale<UE8M0>(amax, eps);
+    const float rc = scale_recip<UE8M0>(s);
+    uint32_t codes[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint64_t v[4] = {f2_from_bf16x2(raw[4 * i]), f2_from_bf16x2(raw[4 * i + 1]),
+                               f2_from_bf16x2(raw[4 * i + 2]), f2_from_bf16x2(raw[4 * i + 3])};
+        quant8<UE8M0>(v, s, rc, codes[2 * i], codes[2 * i + 1]);
+    }
+    if (act)
+        st32<V8>(q + off, codes);
+    if (rank == 0 && tid == 0)
+        scales[row] = s;
+}
+
+// silu_and_mul_dynamic_per_token_quant.  The SiLU products must be kept until
+// the row maximum is known and cannot be cheaply recomputed (the SiLU is
+// most of the kernel's instructions), so each lane holds its 32 products in
+// registers across the exchange.  Staging the inputs in shared memory with
+// cp.async instead, to free those registers for more CTAs per SM, measured
+// slower (174 us against 142 us at T = 4096, I = 25600).
+template <bool UE8M0, bool V8>
+__global__ void __launch_bounds__(kCtaThreads, 4) token_silu_kernel(const uint16_t *__restrict__ x,
+                                                                  uint8_t *__restrict__ q,
+                                                                  float *__restrict__ scales, int cols,
+                                                                  int G, int gpc, int C, float eps)
+{
+    __shared__ float part[kTokenMaxCluster * kTokenMaxWarps];
+    const int tid = threadIdx.x, sub = tid & 3, quad = tid >> 2;
+    const int row = blockIdx.x / C, rank = blockIdx.x - row * C;
+    const int g0 = rank * gpc, g = g0 + quad;
+    const bool act = quad < gpc && g < G;
+    const int64_t lo = int64_t(act ? g : g0) * kGroup + sub * kValsPerLane;
+    const uint16_t *pa = x + int64_t(row) * 2 * cols + lo;
+
+    if (C > 1)
+        cluster_arrive_relaxed();
+    wait_for_producer();
+    allow_consumer_launch();
+
+    uint32_t ra[16], rb[16];
+    ld64_stream<V8>(pa, ra);
+    ld64_stream<V8>(pa + cols, rb);
+    uint64_t v[16];
+    float m = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        v[k] = silu_mul2(ra[k], rb[k]);
+        float v0, v1;
+        f2_unpack(v[k], v0, v1);
+        m = absmax3(m, v0, v1);
+    }
+    const float amax = row_max_exchange(act ? m : 0.0f, part, rank, C);
+
+    const float s = group_scale<UE8M0>(amax, eps);
+    const float rc = scale_recip<UE8M0>(s);
+    uint32_t codes[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        quant8<UE8M0>(*reinterpret_cast<const uint64_t(*)[4]>(&v[4 * i]), s, rc, codes[2 * i], codes[2 * i + 1]);
+    if (act)
+        st32<V8>(q + int64_t(row) * cols + lo, codes);
+    if (rank == 0 && tid == 0)
+        scales[row] = s;
+}
+
+}  // namespace fp8q

@@ -141,6 +141,42 @@ FP8Q_API int fp8q_silu_and_mul_per_block_quant(const void *x, void *q, float *sc
                                       int32_t scale_layout, void *stream);
 
 /*
+ * Per-token variants ("Helion-Kernel in vLLM: PyTorch FP8 ohne CUDA",
+ * section "Welche Kernel wurden in vLLM integriert": the three dynamic
+ * per-token kernels listed next to the per-group ones).  The arithmetic is
+ * that of the per-group op of the same name with the group spanning the
+ * whole output row: one scale per token, s = RN32(max(amax_row, eps) / 448)
+ * (ue8m0: rounded up to a power of two), q = e4m3(RN32(v / s)).
+ *   scales  fp32 [T], written (s[t]); 4-byte aligned.
+ *   The output row length (H, or I) must be a multiple of 128, else
+ *   FP8Q_ERR_UNSUPPORTED (the kernels move 128-value chunks); pointers,
+ *   eps and T == 0 as for the per-group calls.
+ * Longest rows: FP8Q_TOKEN_MAX_COLS for the plain and the SiLU variant (a
+ * row is spread over a cluster of up to 8 CTAs), FP8Q_RMS_MAX_H for the
+ * RMSNorm variant; T * ceil(cols / 8192) < 2^31.
+ */
+#define FP8Q_TOKEN_MAX_COLS 65536
+
+/* dynamic_per_token_scaled_fp8_quant: x bf16 [T, H] -> q e4m3 [T, H],
+ * scales [T].  Bit-identical to the stated arithmetic. */
+FP8Q_API int fp8q_dynamic_per_token_scaled_fp8_quant(const void *x, void *q, float *scales, int64_t T,
+                                                     int64_t H, float eps, int32_t ue8m0, void *stream);
+
+/* rms_norm_dynamic_per_token_quant: rms_norm_per_block_quant's residual,
+ * RMSNorm and weight steps (same argument meaning, same exact sum of
+ * squares, scale floor 1e-10), then one scale per row.  eps is the RMSNorm
+ * variance epsilon. */
+FP8Q_API int fp8q_rms_norm_dynamic_per_token_quant(const void *x, void *residual, const void *weight,
+                                                   void *q, float *scales, int64_t T, int64_t H,
+                                                   float eps, int32_t ue8m0, void *stream);
+
+/* silu_and_mul_dynamic_per_token_quant: x bf16 [T, 2I] = [gate | up] ->
+ * q e4m3 [T, I] of SiLU(gate) * up (as silu_and_mul_per_block_quant),
+ * scales [T]. */
+FP8Q_API int fp8q_silu_and_mul_dynamic_per_token_quant(const void *x, void *q, float *scales, int64_t T,
+                                                       int64_t I, float eps, int32_t ue8m0, void *stream);
+
+/*
  * Elementwise fp32 -> float8_e4m3fn with round to nearest even and
  * saturation to +-448 (the rounding every op above applies to its
  * quotients).  v: fp32 [n] read, out: e4m3 [n] written; both 16-byte

@@ -107,6 +107,30 @@ def test_packed_scale_shape():
         assert k * tp * 4 == (((G) + 3) // 4) * (((T) + 3) // 4 * 4) * 4
 
 
+def test_per_token_checks(lib):
+    E, U, M = fq.FP8Q_ERR_INVALID_ARG, fq.FP8Q_ERR_UNSUPPORTED, fq.FP8Q_ERR_MISALIGNED
+    for f in (fq.fp8q_dynamic_per_token_scaled_fp8_quant, fq.fp8q_silu_and_mul_dynamic_per_token_quant):
+        assert f(A, Q, S, -1, 512, 1e-10, 0, None) == E
+        assert f(A, Q, S, 4, 0, 1e-10, 0, None) == E
+        assert f(A, Q, S, 4, 512, 0.0, 0, None) == E
+        assert f(A, Q, S, 4, 500, 1e-10, 0, None) == U                    # not a multiple of 128
+        assert f(A, Q, S, 4, fq.FP8Q_TOKEN_MAX_COLS + 128, 1e-10, 0, None) == U
+        assert f(A + 2, Q, S, 4, 512, 1e-10, 0, None) == M
+        assert f(A, Q + 8, S, 4, 512, 1e-10, 0, None) == M
+        assert f(A, Q, S + 2, 4, 512, 1e-10, 1, None) == M
+        assert f(None, None, None, 0, 512, 1e-10, 1, None) == 0
+        assert f(None, Q, S, 4, 512, 1e-10, 0, None) == E
+    r = fq.fp8q_rms_norm_dynamic_per_token_quant
+    assert r(A, None, A, Q, S, -1, 512, 1e-6, 0, None) == E
+    assert r(A, None, A, Q, S, 4, 500, 1e-6, 0, None) == U
+    assert r(A, None, A, Q, S, 4, fq.FP8Q_RMS_MAX_H + 128, 1e-6, 0, None) == U
+    assert r(A, None, A, Q, S, 4, 512, -1.0, 0, None) == E
+    assert r(A, None, None, Q, S, 4, 512, 1e-6, 0, None) == E
+    assert r(A, A + 8, A, Q, S, 4, 512, 1e-6, 0, None) == M
+    assert r(A, None, A, Q, S + 1, 4, 512, 1e-6, 0, None) == M
+    assert r(None, None, None, None, None, 0, 512, 1e-6, 0, None) == 0
+
+
 def test_rejects_bad_eps(lib):
     E = fq.FP8Q_ERR_INVALID_ARG
     for eps in (0.0, -1.0, float("inf"), float("nan"), 1e-38):

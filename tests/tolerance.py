@@ -57,10 +57,12 @@ def _near_pow2(x: np.ndarray, rtol: float) -> np.ndarray:
     return (np.abs(x - lo) <= rtol * x) | (np.abs(hi - x) <= rtol * x)
 
 
-def check_fused(q_gpu, s_gpu_tg, q_ref, s_ref_tg, s_pre_tg, v_ref, ue8m0: bool, what="") -> dict:
-    """Scales in [T, G] order.  Returns counts; raises AssertionError on failure."""
+def check_fused(q_gpu, s_gpu_tg, q_ref, s_ref_tg, s_pre_tg, v_ref, ue8m0: bool, what="",
+                group: int = GROUP) -> dict:
+    """Scales in [T, G] order (G = 1 with group = the row length for the
+    per-token ops).  Returns counts; raises AssertionError on failure."""
     T, C = q_ref.shape
-    G = C // GROUP
+    G = C // group
     assert q_gpu.shape == q_ref.shape and s_gpu_tg.shape == s_ref_tg.shape == (T, G), what
     flipped = np.zeros((T, G), bool)
     if not ue8m0:
@@ -81,18 +83,18 @@ def check_fused(q_gpu, s_gpu_tg, q_ref, s_ref_tg, s_pre_tg, v_ref, ue8m0: bool, 
                                      f"oracle {s_ref_tg[idx]!r} (pre-rounding {s_pre_tg[idx]!r})")
             flipped = diff
 
-    qg = q_gpu.reshape(T, G, GROUP)
-    qr = q_ref.reshape(T, G, GROUP).copy()
+    qg = q_gpu.reshape(T, G, group)
+    qr = q_ref.reshape(T, G, group).copy()
     if flipped.any():
         assert v_ref is not None, "a UE8M0 flip needs the oracle's values to re-check codes"
-        vr = v_ref.reshape(T, G, GROUP)
+        vr = v_ref.reshape(T, G, group)
         for t, g in np.argwhere(flipped):
-            qr[t, g] = oracle.quant_pairs(vr[t, g], np.full(GROUP, s_gpu_tg[t, g], np.float32))
+            qr[t, g] = oracle.quant_pairs(vr[t, g], np.full(group, s_gpu_tg[t, g], np.float32))
     d = np.abs(ordinal(qg) - ordinal(qr))
     if d.max(initial=0) > 1:
         i = np.unravel_index(np.argmax(d), d.shape)
         raise AssertionError(f"{what}: code off by {d[i]} e4m3 steps at {i}: gpu {qg[i]:#04x} oracle {qr[i]:#04x}")
-    n_diff = int(np.count_nonzero(d)) + GROUP * int(flipped.sum())
+    n_diff = int(np.count_nonzero(d)) + group * int(flipped.sum())
     budget = math.floor(CODE_FRAC * T * C)
     if n_diff > budget:
         raise AssertionError(f"{what}: {n_diff} codes differ (budget {budget} = 1e-4 of {T * C})")
