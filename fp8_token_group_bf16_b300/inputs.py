@@ -1,4 +1,5 @@
-"""Seeded synthetic inputs for the three FP8 quantisation epilogues.
+"""Seeded synthetic inputs for the FP8 quantisation epilogues and the fused
+QK-norm + rotary embedding.
 
 This module only draws numbers.  It holds none of the arithmetic of the
 method (no scale, no rounding to e4m3, no norm, no SiLU), so the CPU oracle
@@ -27,6 +28,7 @@ SEED_RMS_X, SEED_RMS_W, SEED_RMS_R = 2000, 2001, 2002
 SEED_SILU = 3000
 SEED_SWEEP = 4000
 SEED_MIX_SIGMA, SEED_MIX_X = 5000, 5001
+SEED_QK = 6000
 
 SWEEP_T = (1, 4, 16, 64, 256, 1024, 4096, 16384)
 MIX_T = (1, 8, 64, 512, 4096, 16384)
@@ -229,6 +231,41 @@ def lognormal_channel_input(T: int, C: int, seed_x: int, seed_sigma: int = SEED_
 
 def mix_seed(T: int) -> int:
     return SEED_MIX_X + MIX_T.index(T) if T in MIX_T else SEED_MIX_X + 100 + T
+
+
+# --------------------------------------------------------------------------
+# fused_qk_norm_rope case, Qwen3-32B attention shape: 64 query heads and 8
+# key/value heads of 128 values per token; query/key activations with
+# per-channel spread (lognormal channel std), value heads N(0,1); norm
+# weights 1 + 0.1 N(0,1); positions uniform in [0, P); the rotary table a
+# model holds for those positions: row p = (cos(p f_j), sin(p f_j)), j < D/2,
+# f_j = base^(-2j/D), base 1e6 (Qwen3), computed in float64 and rounded to
+# bf16.  The table is an input of the op, like the weights.
+# --------------------------------------------------------------------------
+
+QK_HQ, QK_HKV, QK_D, QK_P = 64, 8, 128, 40960
+
+
+def rotary_table(P: int, D: int = QK_D, base: float = 1e6) -> torch.Tensor:
+    j = torch.arange(D // 2, dtype=torch.float64)
+    freq = base ** (-2.0 * j / D)
+    ang = torch.arange(P, dtype=torch.float64)[:, None] * freq[None, :]
+    return torch.cat([torch.cos(ang), torch.sin(ang)], dim=1).to(torch.bfloat16).contiguous()
+
+
+def qk_norm_rope_input(T: int, Hq: int = QK_HQ, Hkv: int = QK_HKV, D: int = QK_D, P: int = QK_P,
+                       seed: int = SEED_QK):
+    """Returns (qkv bf16 [T, (Hq + 2 Hkv) D], q_weight bf16 [D], k_weight bf16 [D],
+    cos_sin bf16 [P, D], positions int64 [T])."""
+    g = _gen(seed)
+    nqk = (Hq + Hkv) * D
+    sigma = torch.exp(torch.randn(nqk, generator=g) * 0.5)
+    qkv = torch.randn(T, (Hq + 2 * Hkv) * D, generator=g)
+    qkv[:, :nqk] *= sigma
+    qw = 1.0 + 0.1 * torch.randn(D, generator=g)
+    kw = 1.0 + 0.1 * torch.randn(D, generator=g)
+    pos = torch.randint(0, P, (T,), generator=g, dtype=torch.int64)
+    return bf16(qkv), bf16(qw), bf16(kw), rotary_table(P, D), pos
 
 
 __all__ = [n for n in dir() if not n.startswith("_") and n not in ("annotations", "torch")]

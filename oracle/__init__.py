@@ -100,6 +100,8 @@ def _configure(L: ctypes.CDLL) -> ctypes.CDLL:
     for name in ("oracle_per_token_group_quant", "oracle_rms_norm_per_block_quant",
                  "oracle_silu_and_mul_per_block_quant"):
         getattr(L, name).restype = I
+    L.oracle_fused_qk_norm_rope.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, F, I]
+    L.oracle_fused_qk_norm_rope.restype = I
     L.oracle_pack_ue8m0.argtypes = [P, I64, I64, P]
     L.oracle_pack_ue8m0.restype = I
     L.oracle_f32_to_e4m3_n.argtypes = [P, P, I64]
@@ -225,6 +227,23 @@ def silu_and_mul_dynamic_per_token_quant(x_bits, eps=SCALE_EPS, ue8m0=False, wan
     out = silu_and_mul_per_block_quant(x, group=x.shape[1] // 2, eps=eps, ue8m0=ue8m0,
                                        want_values=want_values)
     return (out[0], out[1][:, 0].copy(), out[2][:, 0].copy()) + tuple(out[3:])
+
+
+def fused_qk_norm_rope(qkv_bits, q_w_bits, k_w_bits, cos_sin_bits, positions, num_q_heads, num_kv_heads,
+                       head_dim=128, eps=RMS_EPS, is_neox=True):
+    """fused_qk_norm_rope ("Helion-Kernel in vLLM: PyTorch FP8 ohne CUDA", the
+    kernel list): per-head RMSNorm of the query and key heads, then the rotary
+    embedding (steps in fp8q_oracle.c).  qkv_bits uint16 [T, (Hq + 2 Hkv) * D];
+    returns the updated copy (value heads unchanged)."""
+    out = np.array(_u16(qkv_bits), copy=True)
+    T = out.shape[0]
+    cs = _u16(cos_sin_bits)
+    pos = np.ascontiguousarray(positions, dtype=np.int64)
+    assert pos.shape == (T,) and out.shape[1] == (num_q_heads + 2 * num_kv_heads) * head_dim
+    _check(lib().oracle_fused_qk_norm_rope(_p(out), _p(_u16(q_w_bits)), _p(_u16(k_w_bits)), _p(cs), _p(pos), T,
+                                           num_q_heads, num_kv_heads, head_dim, cs.shape[0], float(eps),
+                                           int(is_neox)))
+    return out
 
 
 def pack_ue8m0(scales_tg) -> np.ndarray:

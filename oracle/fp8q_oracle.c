@@ -343,6 +343,73 @@ int oracle_silu_and_mul_per_block_quant(const uint16_t *x, uint8_t *q, float *sc
     return ORACLE_OK;
 }
 
+/* ------------------------------------------ fused_qk_norm_rope (f4) -- */
+
+/*
+ * fused_qk_norm_rope ("Helion-Kernel in vLLM: PyTorch FP8 ohne CUDA",
+ * section "Welche Kernel wurden in vLLM integriert", and its speed-up in
+ * "Leistung auf Kernel-Ebene"; the pages give the name only).  The plain
+ * reading of the name, as Qwen3 attention uses it: per-head RMSNorm of the
+ * query and key heads ("QK norm", one weight vector of length D for all query
+ * heads, another for all key heads), then the rotary position embedding of
+ * each normalised head, written back in place; the value heads are not
+ * touched.  Per token t and head h (Hq query heads, then Hkv key heads, then
+ * Hkv value heads, each D contiguous bf16 values):
+ *
+ *   z_i   = x_i                                   (bf16 -> fp32, exact)
+ *   ss    = (float) sum_i z_i^2                   (double, rounded once)
+ *   inv   = RN32(1 / RN32(sqrt(RN32(RN32(ss / D) + eps))))   (as op B)
+ *   y_i   = RN32( RN32(z_i * inv) * w_i )         (w = q_weight or k_weight)
+ *   c_j, s_j = cos_sin[pos_t][j], cos_sin[pos_t][D/2 + j], j < D/2 (bf16)
+ *   pairs (a, b) = (y_j, y_{j+D/2}) (neox style) or (y_{2j}, y_{2j+1})
+ *   a' = RN32( RN32(a * c_j) - RN32(b * s_j) )
+ *   b' = RN32( RN32(b * c_j) + RN32(a * s_j) )
+ *   x  <- bf16_RNE(a'), bf16_RNE(b')
+ *
+ * cos_sin is bf16 [P, D] (full rotary dimension); every position must lie in
+ * [0, P).
+ */
+int oracle_fused_qk_norm_rope(uint16_t *qkv, const uint16_t *q_w, const uint16_t *k_w,
+                              const uint16_t *cos_sin, const int64_t *positions, int64_t T,
+                              int64_t Hq, int64_t Hkv, int64_t D, int64_t P, float eps, int is_neox)
+{
+    if (T < 0 || Hq < 0 || Hkv < 0 || D <= 0 || D % 2 != 0 || D > ORACLE_MAX_ROW || P <= 0)
+        return ORACLE_ERR_ARG;
+    for (int64_t t = 0; t < T; ++t)
+        if (positions[t] < 0 || positions[t] >= P)
+            return ORACLE_ERR_ARG;
+    const int64_t row = (Hq + 2 * Hkv) * D, half = D / 2;
+    static float y[ORACLE_MAX_ROW];
+    for (int64_t t = 0; t < T; ++t) {
+        const uint16_t *cs = cos_sin + positions[t] * D;
+        for (int64_t h = 0; h < Hq + Hkv; ++h) {
+            uint16_t *x = qkv + t * row + h * D;
+            const uint16_t *w = h < Hq ? q_w : k_w;
+            double acc = 0.0;
+            for (int64_t i = 0; i < D; ++i) {
+                double z = (double)oracle_bf16_to_f32(x[i]);
+                acc += z * z;
+            }
+            float inv = oracle_rms_inv((float)acc, D, eps);
+            for (int64_t i = 0; i < D; ++i) {
+                float n = oracle_bf16_to_f32(x[i]) * inv;
+                y[i] = n * oracle_bf16_to_f32(w[i]);
+            }
+            for (int64_t j = 0; j < half; ++j) {
+                const int64_t ia = is_neox ? j : 2 * j;
+                const int64_t ib = is_neox ? j + half : 2 * j + 1;
+                float c = oracle_bf16_to_f32(cs[j]);
+                float sn = oracle_bf16_to_f32(cs[half + j]);
+                float a = y[ia], b = y[ib];
+                float ac = a * c, bs = b * sn, bc = b * c, as = a * sn;
+                x[ia] = oracle_f32_to_bf16(ac - bs);
+                x[ib] = oracle_f32_to_bf16(bc + as);
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
 /* ---------------------------------------------- packed UE8M0 scales -- */
 
 /*

@@ -57,6 +57,13 @@ int oracle_silu_and_mul_per_block_quant(const uint16_t *x, uint8_t *q, float *sc
                                         float *scales_pre, float *v_out, int64_t T, int64_t I,
                                         int64_t gs, float eps, int ue8m0, int col_major);
 
+/* fused_qk_norm_rope: qkv bf16 [T, (Hq + 2*Hkv) * D] in/out (query and key
+ * heads normalised and rotated in place, value heads untouched), q_w / k_w
+ * bf16 [D], cos_sin bf16 [P, D] (cos | sin halves), positions [T] in [0, P). */
+int oracle_fused_qk_norm_rope(uint16_t *qkv, const uint16_t *q_w, const uint16_t *k_w,
+                              const uint16_t *cos_sin, const int64_t *positions, int64_t T,
+                              int64_t Hq, int64_t Hkv, int64_t D, int64_t P, float eps, int is_neox);
+
 /* Packed UE8M0 scales (layout in fp8q_oracle.c): scales_tg fp32 [T,G]
  * row-major powers of two -> ceil(G/4) * round_up(T,4) * 4 bytes. */
 int oracle_pack_ue8m0(const float *scales_tg, int64_t T, int64_t G, uint8_t *out);

@@ -700,6 +700,104 @@ def pin_silu_per_token_bruteforce():
             assert d.max() <= 1 and (d > 0).sum() <= 2, (t, d.max())
 
 
+# ------------------------------------------------ fused_qk_norm_rope ----
+
+
+def _exact_qk_rope(xb, qwb, kwb, csb, pos, Hq, Hkv, D, is_neox, eps=RMS_EPS):
+    """The op in exact rationals with one RN32 per written step."""
+    out = xb.copy()
+    half = D // 2
+    qw = [bf16_to_float(int(b)) for b in qwb]
+    kw = [bf16_to_float(int(b)) for b in kwb]
+    for t in range(xb.shape[0]):
+        cs = [bf16_to_float(int(b)) for b in csb[pos[t]]]
+        for h in range(Hq + Hkv):
+            z = [bf16_to_float(int(b)) for b in xb[t, h * D : (h + 1) * D]]
+            w = qw if h < Hq else kw
+            ss = rn32(sum(Fraction(v) * Fraction(v) for v in z))
+            inv = _exact_inv(ss, D, eps)
+            y = [rn32(Fraction(rn32(Fraction(zz) * Fraction(inv))) * Fraction(ww)) for zz, ww in zip(z, w)]
+            for j in range(half):
+                ia, ib = (j, j + half) if is_neox else (2 * j, 2 * j + 1)
+                c, sn = Fraction(cs[j]), Fraction(cs[half + j])
+                a, b = Fraction(y[ia]), Fraction(y[ib])
+                a2 = rn32(Fraction(rn32(a * c)) - Fraction(rn32(b * sn)))
+                b2 = rn32(Fraction(rn32(b * c)) + Fraction(rn32(a * sn)))
+                out[t, h * D + ia] = np.float32(_bf16_rn(a2)).view(np.uint32) >> 16
+                out[t, h * D + ib] = np.float32(_bf16_rn(b2)).view(np.uint32) >> 16
+    return out
+
+
+def _qk_case(T, Hq, Hkv, D, P, seed):
+    qkv, qw, kw, cs, pos = inputs.qk_norm_rope_input(T, Hq, Hkv, D, P, seed=seed)
+    return inputs.bits(qkv), inputs.bits(qw), inputs.bits(kw), inputs.bits(cs), pos.numpy()
+
+
+def pin_qk_rope_bruteforce():
+    """Both pairings on small heads against the exact-rational transcription."""
+    for is_neox in (True, False):
+        xb, qw, kw, cs, pos = _qk_case(3, 2, 1, 16, 64, seed=71 + is_neox)
+        got = oracle.fused_qk_norm_rope(xb, qw, kw, cs, pos, 2, 1, head_dim=16, is_neox=is_neox)
+        want = _exact_qk_rope(xb, qw, kw, cs, pos, 2, 1, 16, is_neox)
+        bad = np.argwhere(got != want)
+        assert bad.size == 0, (is_neox, bad[:4])
+
+
+def pin_qk_rope_position_zero_is_the_norm():
+    """At position 0 the rotation is the identity (cos 1, sin 0), so the op is
+    the per-head RMSNorm times the weight, rounded to bf16: checked against a
+    float64 evaluation (within one bf16 step) and the value heads unchanged."""
+    Hq, Hkv, D = 4, 2, 128
+    xb, qw, kw, cs, pos = _qk_case(5, Hq, Hkv, D, 16, seed=73)
+    pos[:] = 0
+    got = oracle.fused_qk_norm_rope(xb, qw, kw, cs, pos, Hq, Hkv, head_dim=D)
+    x = bf16_bits_to_f32(xb).astype(np.float64).reshape(5, Hq + 2 * Hkv, D)
+    w = np.concatenate([np.tile(bf16_bits_to_f32(qw), (Hq, 1)), np.tile(bf16_bits_to_f32(kw), (Hkv, 1))])
+    qk = x[:, : Hq + Hkv]
+    ref = qk / np.sqrt((qk * qk).mean(axis=2, keepdims=True) + float(RMS_EPS)) * w[None]
+    g = bf16_bits_to_f32(got).astype(np.float64).reshape(5, Hq + 2 * Hkv, D)
+    assert np.all(np.abs(g[:, : Hq + Hkv] - ref) <= 2.0**-7 * np.abs(ref) + 1e-30)
+    assert np.array_equal(got[:, (Hq + Hkv) * D :], xb[:, (Hq + Hkv) * D :])
+
+
+def pin_qk_rope_pairings_are_a_permutation():
+    """The neox pairing (j, j + D/2) and the interleaved pairing (2j, 2j + 1)
+    are the same rotation on permuted dimensions: interleaving the input and
+    the weights maps one result onto the other, bit for bit."""
+    Hq, Hkv, D = 3, 1, 64
+    xb, qw, kw, cs, pos = _qk_case(4, Hq, Hkv, D, 32, seed=75)
+    perm = np.empty(D, np.int64)
+    perm[0::2] = np.arange(D // 2)
+    perm[1::2] = np.arange(D // 2) + D // 2          # interleaved position i holds neox dim perm[i]
+    heads = Hq + 2 * Hkv
+    x3 = xb.reshape(4, heads, D)
+    xg = np.ascontiguousarray(x3[:, :, perm].reshape(4, heads * D))
+    n = oracle.fused_qk_norm_rope(xb, qw, kw, cs, pos, Hq, Hkv, head_dim=D, is_neox=True)
+    gj = oracle.fused_qk_norm_rope(xg, np.ascontiguousarray(qw[perm]), np.ascontiguousarray(kw[perm]), cs, pos,
+                                   Hq, Hkv, head_dim=D, is_neox=False)
+    assert np.array_equal(gj.reshape(4, heads, D), n.reshape(4, heads, D)[:, :, perm])
+
+
+def pin_qk_rope_rotation_keeps_pair_norms():
+    """Each rotated pair keeps its length (cos^2 + sin^2 = 1 up to the bf16
+    table, 2^-7), and rotating by the angle of position p moves the pair by
+    that angle: the products with the table row give back the normed pair."""
+    Hq, Hkv, D = 2, 1, 128
+    xb, qw, kw, cs, pos = _qk_case(6, Hq, Hkv, D, 4096, seed=77)
+    z = oracle.fused_qk_norm_rope(xb, qw, kw, cs, np.zeros_like(pos), Hq, Hkv, head_dim=D)
+    r = oracle.fused_qk_norm_rope(xb, qw, kw, cs, pos, Hq, Hkv, head_dim=D)
+    zf = bf16_bits_to_f32(z).astype(np.float64).reshape(6, -1, D)[:, : Hq + Hkv]
+    rf = bf16_bits_to_f32(r).astype(np.float64).reshape(6, -1, D)[:, : Hq + Hkv]
+    h = D // 2
+    nz = np.hypot(zf[..., :h], zf[..., h:])
+    nr = np.hypot(rf[..., :h], rf[..., h:])
+    assert np.all(np.abs(nr - nz) <= 2.0**-6 * nz + 1e-30)
+    c = bf16_bits_to_f32(cs)[pos][:, None, :h].astype(np.float64)
+    sn = bf16_bits_to_f32(cs)[pos][:, None, h:].astype(np.float64)
+    a = rf[..., :h] * c + rf[..., h:] * sn            # rotate back
+    assert np.all(np.abs(a - zf[..., :h]) <= 2.0**-5 * nz + 1e-30)
+
+
 ALL_PINS = [
     pin_golden_midpoints,
     pin_ue8m0_packed_golden,
@@ -725,6 +823,10 @@ ALL_PINS = [
     pin_per_token_row_amax,
     pin_rms_per_token_bruteforce,
     pin_silu_per_token_bruteforce,
+    pin_qk_rope_bruteforce,
+    pin_qk_rope_position_zero_is_the_norm,
+    pin_qk_rope_pairings_are_a_permutation,
+    pin_qk_rope_rotation_keeps_pair_norms,
     pin_e4m3_structured_exact,
     pin_ue8m0,
     pin_e4m3_torch_cast,

@@ -13,6 +13,30 @@ import oracle
 import pins
 
 MUTATIONS = {
+    "rope_sign_of_sine_term_flipped": (
+        "x[ia] = oracle_f32_to_bf16(ac - bs);",
+        "x[ia] = oracle_f32_to_bf16(ac + bs);",
+    ),
+    "rope_cos_and_sin_swapped": (
+        "float c = oracle_bf16_to_f32(cs[j]);\n                float sn = oracle_bf16_to_f32(cs[half + j]);",
+        "float c = oracle_bf16_to_f32(cs[half + j]);\n                float sn = oracle_bf16_to_f32(cs[j]);",
+    ),
+    "rope_neox_partner_adjacent": (
+        "const int64_t ib = is_neox ? j + half : 2 * j + 1;",
+        "const int64_t ib = is_neox ? 2 * j + 1 : 2 * j + 1;",
+    ),
+    "qk_norm_query_weight_on_key_heads": (
+        "const uint16_t *w = h < Hq ? q_w : k_w;",
+        "const uint16_t *w = q_w;",
+    ),
+    "qk_norm_mean_over_half_head": (
+        "float inv = oracle_rms_inv((float)acc, D, eps);",
+        "float inv = oracle_rms_inv((float)acc, D / 2, eps);",
+    ),
+    "rope_first_token_position_for_all": (
+        "const uint16_t *cs = cos_sin + positions[t] * D;",
+        "const uint16_t *cs = cos_sin + positions[0] * D;",
+    ),
     "amax_over_first_128_values_only": (
         "for (int64_t i = 0; i < gs; ++i) {\n        float a = fabsf(v[i]);",
         "for (int64_t i = 0; i < (gs < 128 ? gs : 128); ++i) {\n        float a = fabsf(v[i]);",
