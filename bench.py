@@ -87,6 +87,13 @@ def algorithmic_bytes(op: str, T: int, H: int, residual: bool = False, packed: b
     raise ValueError(op)
 
 
+def qk_rope_bytes(T: int, Hq: int = 64, Hkv: int = 8, D: int = 128) -> int:
+    """fused_qk_norm_rope: every query and key head read and written once
+    (bf16), each token's position (8 B) and its cos/sin table row (2D bf16),
+    and the two norm weights once per launch; value heads are not touched."""
+    return T * ((Hq + Hkv) * D * 4 + 8 + 2 * D) + 4 * D
+
+
 def step_bytes(T: int = STEP_T) -> int:
     return (algorithmic_bytes("per_token_group_fp8_quant", T, A_H)
             + algorithmic_bytes("rms_norm_per_block_quant", T, B_H)
@@ -654,6 +661,30 @@ def sweep(args):
         torch.cuda.empty_cache()
         row = {"op": op, "T": T, "H_or_I": H, "ue8m0": ue8m0, "scales": lay, "residual": res,
                "bytes": nbytes, "us": round(us, 3), "GBps": round(nbytes / us / 1e3, 1),
+               "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "copy_us": round(cus, 3),
+               "copy_GBps": round(nbytes / cus / 1e3, 1), "peak": peak, "peak_kind": peak_kind}
+        rows.append(row)
+        print(json.dumps(row), flush=True)
+
+    # fused_qk_norm_rope, Qwen3-32B attention shape (64 query, 8 key/value heads of 128)
+    from fp8_token_group_bf16_b300 import inputs as _inputs
+    table = _inputs.rotary_table(_inputs.QK_P).to(dev)
+    qw = (1.0 + 0.1 * torch.randn(128, device=dev)).to(torch.bfloat16)
+    kw = (1.0 + 0.1 * torch.randn(128, device=dev)).to(torch.bfloat16)
+    for T in (64, 512, 4096, 16384):
+        nbytes = qk_rope_bytes(T)
+
+        def make(T=T):
+            qkv = torch.randn(T, 80 * 128, device=dev).to(torch.bfloat16)
+            pos = torch.randint(0, _inputs.QK_P, (T,), device=dev, dtype=torch.int64)
+            return lambda: fq.fused_qk_norm_rope(qkv, qw, kw, table, pos, 64, 8)
+
+        iters = 200 if nbytes < 50e6 else 40
+        us = timed(make, nbytes, iters)
+        cus = timed(copy_maker(nbytes), nbytes, iters)
+        torch.cuda.empty_cache()
+        row = {"op": "fused_qk_norm_rope", "T": T, "H_or_I": "64q+8kv x 128", "ue8m0": None, "scales": None,
+               "residual": False, "bytes": nbytes, "us": round(us, 3), "GBps": round(nbytes / us / 1e3, 1),
                "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "copy_us": round(cus, 3),
                "copy_GBps": round(nbytes / cus / 1e3, 1), "peak": peak, "peak_kind": peak_kind}
         rows.append(row)

@@ -7,13 +7,15 @@ The compute lives in ``libfp8q.so`` (hand-written CUDA for sm_103a, C ABI in
   ``fp8q_silu_and_mul_per_block_quant``, their per-token variants
   ``fp8q_dynamic_per_token_scaled_fp8_quant``,
   ``fp8q_rms_norm_dynamic_per_token_quant``,
-  ``fp8q_silu_and_mul_dynamic_per_token_quant``, and ``fp8q_f32_to_e4m3``,
+  ``fp8q_silu_and_mul_dynamic_per_token_quant``, ``fp8q_fused_qk_norm_rope``,
+  and ``fp8q_f32_to_e4m3``,
   ``fp8q_status_string`` -- the C entry points under their own names, taking
   raw device pointers (ints) and sizes, returning the status code;
 * ``per_token_group_fp8_quant``, ``rms_norm_per_block_quant``,
   ``silu_and_mul_per_block_quant``, ``dynamic_per_token_scaled_fp8_quant``,
   ``rms_norm_dynamic_per_token_quant``,
-  ``silu_and_mul_dynamic_per_token_quant`` -- the same calls on torch tensors:
+  ``silu_and_mul_dynamic_per_token_quant``, ``fused_qk_norm_rope`` -- the
+  same calls on torch tensors:
   argument checks, output allocation, the current CUDA stream, and an
   exception on a non-zero status.  Every step of the computation runs in the
   library's kernels; there is no CPU fallback.  If the library is missing or
@@ -49,6 +51,7 @@ EXPORTS = (
     "fp8q_dynamic_per_token_scaled_fp8_quant",
     "fp8q_rms_norm_dynamic_per_token_quant",
     "fp8q_silu_and_mul_dynamic_per_token_quant",
+    "fp8q_fused_qk_norm_rope",
     "fp8q_f32_to_e4m3",
     "fp8q_status_string",
     "fp8q_version",
@@ -80,8 +83,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.fp8q_dynamic_per_token_scaled_fp8_quant.argtypes = [P, P, P, I64, I64, F, I32, P]
     L.fp8q_rms_norm_dynamic_per_token_quant.argtypes = [P, P, P, P, P, I64, I64, F, I32, P]
     L.fp8q_silu_and_mul_dynamic_per_token_quant.argtypes = [P, P, P, I64, I64, F, I32, P]
+    L.fp8q_fused_qk_norm_rope.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, F, I32, P]
     L.fp8q_f32_to_e4m3.argtypes = [P, P, I64, P]
-    for n in EXPORTS[:7]:
+    for n in EXPORTS[:8]:
         getattr(L, n).restype = ctypes.c_int
     L.fp8q_status_string.argtypes = [ctypes.c_int]
     L.fp8q_status_string.restype = ctypes.c_char_p
@@ -122,6 +126,12 @@ def fp8q_rms_norm_dynamic_per_token_quant(x, residual, weight, q, scales, T, H, 
 
 def fp8q_silu_and_mul_dynamic_per_token_quant(x, q, scales, T, I, eps, ue8m0, stream):
     return load().fp8q_silu_and_mul_dynamic_per_token_quant(x, q, scales, T, I, eps, ue8m0, stream)
+
+
+def fp8q_fused_qk_norm_rope(qkv, q_weight, k_weight, cos_sin, positions, T, num_q_heads, num_kv_heads,
+                            head_dim, max_position, eps, is_neox, stream):
+    return load().fp8q_fused_qk_norm_rope(qkv, q_weight, k_weight, cos_sin, positions, T, num_q_heads,
+                                          num_kv_heads, head_dim, max_position, eps, is_neox, stream)
 
 
 def fp8q_f32_to_e4m3(v, out, n, stream):
@@ -332,6 +342,32 @@ def silu_and_mul_dynamic_per_token_quant(x, eps: float = 1e-10, ue8m0: bool = Fa
                                                      int(ue8m0), _stream_ptr(x, stream)),
            "silu_and_mul_dynamic_per_token_quant")
     return q, scales
+
+
+# ------------------------------------------------- fused_qk_norm_rope ----
+
+
+def fused_qk_norm_rope(qkv, q_weight, k_weight, cos_sin, positions, num_q_heads: int, num_kv_heads: int,
+                       head_dim: int = 128, eps: float = 1e-6, is_neox: bool = True, stream=None):
+    """In place on qkv bf16 [T, (Hq + 2 Hkv) * D]: RMSNorm of every query and
+    key head (weights q_weight / k_weight, bf16 [D]), then the rotary
+    embedding from cos_sin bf16 [max_position, D] at positions int64 [T].
+    Value heads are left as they are.  Returns qkv."""
+    torch = _torch()
+    for name, t in (("qkv", qkv), ("q_weight", q_weight), ("k_weight", k_weight), ("cos_sin", cos_sin)):
+        _need_cuda_bf16(name, t)
+    if positions.device != qkv.device or positions.dtype != torch.int64 or not positions.is_contiguous():
+        raise ValueError("positions must be a contiguous int64 tensor on the device of qkv")
+    T = qkv.shape[0]
+    if qkv.dim() != 2 or qkv.shape[1] != (num_q_heads + 2 * num_kv_heads) * head_dim:
+        raise ValueError("qkv must be [T, (num_q_heads + 2 * num_kv_heads) * head_dim]")
+    if positions.numel() != T or q_weight.numel() != head_dim or k_weight.numel() != head_dim or \
+            cos_sin.dim() != 2 or cos_sin.shape[1] != head_dim:
+        raise ValueError("positions [T], weights [head_dim] and cos_sin [max_position, head_dim] expected")
+    _check(fp8q_fused_qk_norm_rope(qkv.data_ptr(), q_weight.data_ptr(), k_weight.data_ptr(), cos_sin.data_ptr(),
+                                   positions.data_ptr(), T, num_q_heads, num_kv_heads, head_dim, cos_sin.shape[0],
+                                   eps, int(is_neox), _stream_ptr(qkv, stream)), "fused_qk_norm_rope")
+    return qkv
 
 
 def f32_to_e4m3(v, out=None, stream=None):

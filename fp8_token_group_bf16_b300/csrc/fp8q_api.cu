@@ -3,6 +3,7 @@
 #include "fp8q.h"
 #include "fp8q_kernels.cuh"
 #include "fp8q_rms.cuh"
+#include "fp8q_rope.cuh"
 #include "fp8q_token.cuh"
 
 #include <cmath>
@@ -373,6 +374,46 @@ int fp8q_rms_norm_dynamic_per_token_quant(const void *x, void *residual, const v
         : launch_rms<U, kPerToken, false>(xp, rp, wp, qp, scales, t, h, G, eps, st))
     e = ue8m0 ? FP8Q_RMS(true) : FP8Q_RMS(false);
 #undef FP8Q_RMS
+    return launch_status(e);
+}
+
+int fp8q_fused_qk_norm_rope(void *qkv, const void *q_weight, const void *k_weight, const void *cos_sin,
+                            const int64_t *positions, int64_t T, int64_t num_q_heads, int64_t num_kv_heads,
+                            int64_t head_dim, int64_t max_position, float eps, int32_t is_neox, void *stream)
+{
+    if (T < 0 || num_q_heads < 0 || num_kv_heads < 0 || head_dim <= 0 || max_position <= 0 ||
+        !std::isfinite(eps) || eps < 0.0f)
+        return FP8Q_ERR_INVALID_ARG;
+    if (head_dim != kHeadDim)
+        return FP8Q_ERR_UNSUPPORTED;
+    const int64_t nh = num_q_heads + num_kv_heads;
+    if (T == 0 || nh == 0)
+        return FP8Q_OK;
+    if (!qkv || !q_weight || !k_weight || !cos_sin || !positions)
+        return FP8Q_ERR_INVALID_ARG;
+    if (!aligned(qkv, 16) || !aligned(q_weight, 16) || !aligned(k_weight, 16) || !aligned(cos_sin, 16) ||
+        !aligned(positions, 8))
+        return FP8Q_ERR_MISALIGNED;
+    const int64_t n = T * nh;
+    if (nh >= (int64_t(1) << 20) || n / nh != T || n >= (int64_t(1) << 31))
+        return FP8Q_ERR_UNSUPPORTED;
+    const int64_t row = (num_q_heads + 2 * num_kv_heads) * head_dim;
+    const bool v8 = aligned(qkv, 32) && aligned(q_weight, 32) && aligned(k_weight, 32) && aligned(cos_sin, 32);
+    auto x = static_cast<uint16_t *>(qkv);
+    auto qw = static_cast<const uint16_t *>(q_weight);
+    auto kw = static_cast<const uint16_t *>(k_weight);
+    auto cs = static_cast<const uint16_t *>(cos_sin);
+    const dim3 grid{unsigned((n + 63) / 64)}, block{256};
+    auto st = static_cast<cudaStream_t>(stream);
+    const int nhi = int(nh), hq = int(num_q_heads);
+    cudaError_t e;
+#define FP8Q_ROPE(N, V) launch(qk_norm_rope_kernel<N, V>, grid, block, st, x, qw, kw, cs, positions, n, nhi, hq, row, \
+                               max_position, eps)
+    if (is_neox)
+        e = v8 ? FP8Q_ROPE(true, true) : FP8Q_ROPE(true, false);
+    else
+        e = v8 ? FP8Q_ROPE(false, true) : FP8Q_ROPE(false, false);
+#undef FP8Q_ROPE
     return launch_status(e);
 }
 

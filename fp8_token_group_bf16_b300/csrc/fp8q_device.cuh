@@ -265,6 +265,11 @@ __device__ __forceinline__ float scale_recip(float s)
 //
 // add/sub/mul/fma .rn.f32x2 round each half exactly like the scalar
 // instruction; one packed instruction takes one issue slot for two values.
+// A packed multiply whose product feeds a packed add or subtract can be
+// fused into one multiply-add by the code generator (measured: the rotation
+// of the fused QK-norm + RoPE kernel); the kernels use that pattern only
+// where the product is exact (squares of bf16 values), and the scalar
+// __fmul_rn / __fadd_rn intrinsics, which are never fused, elsewhere.
 
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
 {

@@ -1,0 +1,175 @@
+// fused_qk_norm_rope for sm_103a: per-head RMSNorm of the query and key heads
+// followed by the rotary position embedding, in place on the packed qkv
+// projection ("Helion-Kernel in vLLM: PyTorch FP8 ohne CUDA", section
+// "Welche Kernel wurden in vLLM integriert").
+//
+// A head of 128 values is owned by a quad, as a quantisation group is: 32
+// values per lane, the exact sum of squares of fp8q_rms.cuh per lane and
+// TwoSum across the quad, so 1/rms is bit-identical to a sequential
+// evaluation with the sum carried in double.  The lanes take the values so
+// that every rotation pair stays inside one lane:
+//   neox pairing (j, j + 64):      lane s holds dims 16s..16s+15 and
+//                                  64+16s..64+16s+15 (two 32-byte pieces);
+//   interleaved pairing (2j, 2j+1): lane s holds dims 32s..32s+31.
+// Either way lane s uses cos/sin entries j = 16s..16s+15 of the position's
+// table row.  Every step is one correctly rounded fp32 operation, in the
+// order y = (z * inv) * w, a' = a c - b s, b' = b c + a s, then bf16
+// round-to-nearest-even, so the result is bit-exact.
+#pragma once
+
+#include "fp8q_device.cuh"
+#include "fp8q_exact.cuh"
+#include "fp8q_rms.cuh"
+
+namespace fp8q {
+
+constexpr int kHeadDim = 128;
+
+// 32 bytes (16 bf16) that this kernel also writes: coherent path.
+template <bool V8>
+__device__ __forceinline__ void ld32_rw(const void *p, uint32_t *w)
+{
+    const char *c = static_cast<const char *>(p);
+    if (V8) {
+        FP8Q_LD8(".L1::no_allocate", c, w, 0);
+    } else {
+        FP8Q_LD4(".L1::no_allocate", c, w[0], w[1], w[2], w[3]);
+        FP8Q_LD4(".L1::no_allocate", c + 16, w[4], w[5], w[6], w[7]);
+    }
+}
+
+// 32 bytes of a small table every CTA reads (weights, cos/sin rows): L1.
+template <bool V8>
+__device__ __forceinline__ void ld32_table(const void *p, uint32_t *w)
+{
+    const char *c = static_cast<const char *>(p);
+    if (V8) {
+        FP8Q_LD8(".nc.L2::evict_last", c, w, 0);
+    } else {
+        FP8Q_LD4(".nc", c, w[0], w[1], w[2], w[3]);
+        FP8Q_LD4(".nc", c + 16, w[4], w[5], w[6], w[7]);
+    }
+}
+
+template <bool V8>
+__device__ __forceinline__ void st32_words(void *p, const uint32_t *w)
+{
+    char *c = static_cast<char *>(p);
+    if (V8) {
+        asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(c), "r"(w[0]), "r"(w[1]),
+                     "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                     : "memory");
+    } else {
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+            asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(c + 16 * k), "r"(w[4 * k]),
+                         "r"(w[4 * k + 1]), "r"(w[4 * k + 2]), "r"(w[4 * k + 3])
+                         : "memory");
+    }
+}
+
+// Two fp32 values -> bf16x2 (low half = lo), round to nearest even.
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Grid: one quad per (token, head) unit over the T * (Hq + Hkv) query and key
+// heads, flat (unit u: token u / nh, head u % nh, nh = Hq + Hkv); 64 units
+// per CTA of 256 threads.  Positions outside [0, P) are clamped into the
+// table (the result for such a token is unspecified, the access stays in
+// bounds).
+template <bool NEOX, bool V8>
+__global__ void __launch_bounds__(256) qk_norm_rope_kernel(uint16_t *__restrict__ qkv,
+                                                           const uint16_t *__restrict__ q_w,
+                                                           const uint16_t *__restrict__ k_w,
+                                                           const uint16_t *__restrict__ cos_sin,
+                                                           const int64_t *__restrict__ positions, int64_t n_units,
+                                                           int nh, int Hq, int64_t row, int64_t P, float eps)
+{
+    const int sub = threadIdx.x & 3;
+    const int64_t u = int64_t(blockIdx.x) * 64 + (threadIdx.x >> 2);
+    const int64_t ul = u < n_units ? u : n_units - 1;
+    const uint32_t t = uint32_t(ul) / uint32_t(nh), h = uint32_t(ul) - t * uint32_t(nh);
+    uint16_t *xh = qkv + int64_t(t) * row + int64_t(h) * kHeadDim;
+    const uint16_t *w = h < uint32_t(Hq) ? q_w : k_w;
+    // element offsets of the lane's two 16-value pieces
+    const int o0 = NEOX ? 16 * sub : 32 * sub;
+    const int o1 = NEOX ? 64 + 16 * sub : 32 * sub + 16;
+
+    wait_for_producer();
+    allow_consumer_launch();
+
+    uint32_t z[16], wr[16], cs[16];
+    ld32_rw<V8>(xh + o0, z);
+    ld32_rw<V8>(xh + o1, z + 8);
+    int64_t pos = positions[t];
+    pos = pos < 0 ? 0 : (pos >= P ? P - 1 : pos);
+    const uint16_t *crow = cos_sin + pos * kHeadDim;
+    ld32_table<V8>(w + o0, wr);
+    ld32_table<V8>(w + o1, wr + 8);
+    ld32_table<V8>(crow + 16 * sub, cs);            // cos_j, j = 16 sub ..
+    ld32_table<V8>(crow + 64 + 16 * sub, cs + 8);   // sin_j
+
+    // ---- 1/rms of the head: exact lane sums, TwoSum across the quad
+    float hi, lo;
+    lane_sumsq(z, hi, lo);
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1)
+        pair_add(hi, lo, __shfl_xor_sync(0xFFFFFFFFu, hi, o), __shfl_xor_sync(0xFFFFFFFFu, lo, o));
+    const float inv = rms_inv(hi, lo, kHeadDim, eps);
+    const uint64_t inv2 = f2_pack(inv, inv);
+
+    // ---- y = (z * inv) * w, then the rotation of each (a, b) pair
+    uint32_t out[16];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        // table word k holds cos (or sin) of j = 16 sub + 2k and 2k + 1
+        const uint64_t c = f2_from_bf16x2(cs[k]), s = f2_from_bf16x2(cs[8 + k]);
+        uint64_t a, b;
+        if (NEOX) {
+            // z word k: dims 16 sub + 2k, +1 (first half); word 8 + k: the partners
+            a = f2_mul(f2_mul(f2_from_bf16x2(z[k]), inv2), f2_from_bf16x2(wr[k]));
+            b = f2_mul(f2_mul(f2_from_bf16x2(z[8 + k]), inv2), f2_from_bf16x2(wr[8 + k]));
+        } else {
+            // z word m holds dims 32 sub + 2m, +1: the pair j = 16 sub + m; words
+            // 2k, 2k+1 are the pairs j = 16 sub + 2k and j + 1, (a0, b0), (a1, b1)
+            const int k0 = 2 * k;
+            const uint64_t y0 = f2_mul(f2_mul(f2_from_bf16x2(z[k0]), inv2), f2_from_bf16x2(wr[k0]));
+            const uint64_t y1 = f2_mul(f2_mul(f2_from_bf16x2(z[k0 + 1]), inv2), f2_from_bf16x2(wr[k0 + 1]));
+            float a0, b0, a1, b1;
+            f2_unpack(y0, a0, b0);
+            f2_unpack(y1, a1, b1);
+            a = f2_pack(a0, a1);
+            b = f2_pack(b0, b1);
+        }
+        // The rotation in scalar IEEE intrinsics: the code generator may fuse a
+        // packed multiply into a following packed add or subtract (one
+        // rounding instead of two), which __fmul_rn / __fadd_rn / __fsub_rn
+        // are guaranteed never to be.
+        float ya0, ya1, yb0, yb1, c0, c1, s0, s1;
+        f2_unpack(a, ya0, ya1);
+        f2_unpack(b, yb0, yb1);
+        f2_unpack(c, c0, c1);
+        f2_unpack(s, s0, s1);
+        const float a0 = __fsub_rn(__fmul_rn(ya0, c0), __fmul_rn(yb0, s0));
+        const float a1 = __fsub_rn(__fmul_rn(ya1, c1), __fmul_rn(yb1, s1));
+        const float b0 = __fadd_rn(__fmul_rn(yb0, c0), __fmul_rn(ya0, s0));
+        const float b1 = __fadd_rn(__fmul_rn(yb1, c1), __fmul_rn(ya1, s1));
+        if (NEOX) {
+            out[k] = bf16x2_rn(a0, a1);
+            out[8 + k] = bf16x2_rn(b0, b1);
+        } else {
+            out[2 * k] = bf16x2_rn(a0, b0);
+            out[2 * k + 1] = bf16x2_rn(a1, b1);
+        }
+    }
+    if (u < n_units) {
+        st32_words<V8>(xh + o0, out);
+        st32_words<V8>(xh + o1, out + 8);
+    }
+}
+
+}  // namespace fp8q

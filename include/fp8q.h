@@ -177,6 +177,35 @@ FP8Q_API int fp8q_silu_and_mul_dynamic_per_token_quant(const void *x, void *q, f
                                                        int64_t I, float eps, int32_t ue8m0, void *stream);
 
 /*
+ * fused_qk_norm_rope ("Helion-Kernel in vLLM: PyTorch FP8 ohne CUDA",
+ * section "Welche Kernel wurden in vLLM integriert"): per-head RMSNorm of
+ * the query and key heads, then the rotary position embedding, in place.
+ *   qkv        bf16 [T, (Hq + 2*Hkv) * D], read and written: per token the
+ *              Hq query heads, then Hkv key heads, then Hkv value heads, D
+ *              values each.  Query and key heads are replaced, value heads
+ *              are not touched.
+ *   q_weight, k_weight  bf16 [D], the norm weights of query and key heads.
+ *   cos_sin    bf16 [max_position, D], row p = (cos_0..cos_{D/2-1},
+ *              sin_0..sin_{D/2-1}) for position p (full rotary dimension).
+ *   positions  int64 [T] (device), each in [0, max_position); a position
+ *              outside is clamped into the table (the access stays in
+ *              bounds; that token's result is unspecified).
+ *   eps        RMSNorm variance epsilon, finite and >= 0.
+ *   is_neox    nonzero: pairs (j, j + D/2); zero: pairs (2j, 2j + 1).
+ * Per head: ss = sum z_i^2 (exact, rounded once), inv = RN32(1/RN32(sqrt(
+ * RN32(RN32(ss/D) + eps)))), y_i = RN32(RN32(z_i inv) w_i); per pair (a, b)
+ * with (c, s) = table[pos][j], table[pos][D/2 + j]: a' = RN32(RN32(a c) -
+ * RN32(b s)), b' = RN32(RN32(b c) + RN32(a s)); the outputs are rounded to
+ * bf16 (nearest even).  Bit-identical to this sequence.  D must be 128
+ * (FP8Q_ERR_UNSUPPORTED otherwise); T * (Hq + Hkv) < 2^31.  Alignment: qkv,
+ * the weights and the table 16 bytes, positions 8 bytes.
+ */
+FP8Q_API int fp8q_fused_qk_norm_rope(void *qkv, const void *q_weight, const void *k_weight, const void *cos_sin,
+                                     const int64_t *positions, int64_t T, int64_t num_q_heads,
+                                     int64_t num_kv_heads, int64_t head_dim, int64_t max_position, float eps,
+                                     int32_t is_neox, void *stream);
+
+/*
  * Elementwise fp32 -> float8_e4m3fn with round to nearest even and
  * saturation to +-448 (the rounding every op above applies to its
  * quotients).  v: fp32 [n] read, out: e4m3 [n] written; both 16-byte

@@ -131,6 +131,23 @@ def test_per_token_checks(lib):
     assert r(None, None, None, None, None, 0, 512, 1e-6, 0, None) == 0
 
 
+def test_qk_norm_rope_checks(lib):
+    E, U, M = fq.FP8Q_ERR_INVALID_ARG, fq.FP8Q_ERR_UNSUPPORTED, fq.FP8Q_ERR_MISALIGNED
+    f = fq.fp8q_fused_qk_norm_rope
+    assert f(A, A, A, A, S, -1, 64, 8, 128, 4096, 1e-6, 1, None) == E
+    assert f(A, A, A, A, S, 4, -1, 8, 128, 4096, 1e-6, 1, None) == E
+    assert f(A, A, A, A, S, 4, 64, 8, 128, 0, 1e-6, 1, None) == E
+    assert f(A, A, A, A, S, 4, 64, 8, 128, 4096, -1.0, 1, None) == E
+    assert f(A, A, A, A, S, 4, 64, 8, 0, 4096, 1e-6, 1, None) == E
+    assert f(A, A, A, A, S, 4, 64, 8, 64, 4096, 1e-6, 1, None) == U       # only 128-value heads
+    assert f(A, A, A, A, S + 4, 4, 64, 8, 128, 4096, 1e-6, 1, None) == M  # positions 8-byte aligned
+    assert f(A + 2, A, A, A, S, 4, 64, 8, 128, 4096, 1e-6, 1, None) == M
+    assert f(A, A, A, A + 8, S, 4, 64, 8, 128, 4096, 1e-6, 0, None) == M
+    assert f(None, A, A, A, S, 4, 64, 8, 128, 4096, 1e-6, 1, None) == E
+    assert f(None, None, None, None, None, 0, 64, 8, 128, 4096, 1e-6, 1, None) == 0
+    assert f(None, None, None, None, None, 4, 0, 0, 128, 4096, 1e-6, 1, None) == 0
+
+
 def test_rejects_bad_eps(lib):
     E = fq.FP8Q_ERR_INVALID_ARG
     for eps in (0.0, -1.0, float("inf"), float("nan"), 1e-38):
