@@ -22,7 +22,10 @@ its own batch (weak scaling, no collective on the data path).
 
 ``--impl reference`` times the CPU oracle instead (the reference arm: this
 method has no published implementation to install).  ``--sweep`` prints
-per-op T sweeps with a same-size device-to-device copy for comparison.
+per-op T sweeps with a same-size device-to-device copy for comparison,
+including the packed-scale layout, the per-token variants and
+fused_qk_norm_rope.  ``--op NAME --tokens T`` times one op alone (for
+profiling one kernel).
 """
 
 from __future__ import annotations
@@ -692,6 +695,82 @@ def sweep(args):
     return rows
 
 
+# ------------------------------------------------------------ one op ------
+
+SINGLE_OPS = {
+    # op: (row length, ue8m0, scale layout)
+    "per_token_group_fp8_quant": (A_H, True, "col"),
+    "rms_norm_per_block_quant": (B_H, True, "row"),
+    "silu_and_mul_per_block_quant": (C_I, True, "row"),
+    "dynamic_per_token_scaled_fp8_quant": (A_H, False, "token"),
+    "rms_norm_dynamic_per_token_quant": (B_H, False, "token"),
+    "silu_and_mul_dynamic_per_token_quant": (C_I, False, "token"),
+    "fused_qk_norm_rope": (None, None, None),
+}
+
+
+def single_op(args):
+    """--op NAME: W warm-up launches, then K launches of one op at T = --tokens
+    on one stream, timed with CUDA events; inputs rotated over enough buffer
+    sets to exceed 3x L2.  One JSON line (op, T, us per launch, GB/s,
+    fraction of the measured copy bandwidth).  Made for profiling one kernel."""
+    import torch
+
+    import fp8_token_group_bf16_b300 as fq
+    from fp8_token_group_bf16_b300 import inputs as _inputs
+
+    fq.load()
+    dev = torch.device("cuda")
+    op, T = args.op, args.tokens
+    H, ue8m0, lay = SINGLE_OPS[op]
+    if op == "fused_qk_norm_rope":
+        nbytes = qk_rope_bytes(T)
+        table = _inputs.rotary_table(_inputs.QK_P).to(dev)
+        w = (1.0 + 0.1 * torch.randn(128, device=dev)).to(torch.bfloat16)
+    else:
+        nbytes = algorithmic_bytes(op, T, H, packed=args.packed)
+    nsets = min(16, max(2, int(3 * (126 << 20) // nbytes) + 1))
+    calls = []
+    for _ in range(nsets):
+        if op == "fused_qk_norm_rope":
+            qkv = torch.randn(T, 80 * 128, device=dev).to(torch.bfloat16)
+            pos = torch.randint(0, _inputs.QK_P, (T,), device=dev, dtype=torch.int64)
+            calls.append(lambda qkv=qkv, pos=pos: fq.fused_qk_norm_rope(qkv, w, w, table, pos, 64, 8))
+            continue
+        x = torch.randn(T, 2 * H if "silu" in op else H, device=dev).to(torch.bfloat16)
+        q = torch.empty(T, H, dtype=torch.float8_e4m3fn, device=dev)
+        if lay == "token":
+            f = getattr(fq, op)
+            if op.startswith("rms"):
+                wt = torch.randn(H, device=dev).to(torch.bfloat16)
+                calls.append(lambda x=x, q=q, wt=wt: fq.rms_norm_dynamic_per_token_quant(x, wt, None, q=q))
+            else:
+                calls.append(lambda x=x, q=q, f=f: f(x, q=q))
+            continue
+        kw = dict(ue8m0=ue8m0 or args.packed, column_major_scales=lay == "col" and not args.packed,
+                  packed_ue8m0_scales=args.packed, q=q)
+        if op.startswith("rms"):
+            wt = torch.randn(H, device=dev).to(torch.bfloat16)
+            calls.append(lambda x=x, wt=wt, kw=kw: fq.rms_norm_per_block_quant(x, wt, None, **kw))
+        else:
+            f = getattr(fq, op)
+            calls.append(lambda x=x, f=f, kw=kw: f(x, **kw))
+    for k in range(args.warmup):
+        calls[k % nsets]()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for k in range(args.steps):
+        calls[k % nsets]()
+    b.record()
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) * 1e3 / args.steps
+    peak, kind = load_peaks()
+    print(json.dumps({"op": op, "T": T, "packed": args.packed, "launches": args.steps, "us": round(us, 3),
+                      "GBps": round(nbytes / us / 1e3, 1), "frac_of_peak": round(nbytes / us / 1e3 / peak, 4),
+                      "peak": peak, "peak_kind": kind}), flush=True)
+
+
 # ------------------------------------------------------------------- main --
 
 
@@ -703,6 +782,9 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--sweep", action="store_true")
+    p.add_argument("--op", choices=sorted(SINGLE_OPS), default=None,
+                   help="time one op at --tokens (K launches after W warm-ups) instead of the step")
+    p.add_argument("--packed", action="store_true", help="with --op: packed UE8M0 scales (per-group ops)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--tokens", type=int, default=STEP_T,
                    help="tokens per step (default: the T=4096 workload; smaller values are for profiling)")
@@ -729,6 +811,10 @@ def main(argv=None):
         if args.sweep:
             if dist.rank == 0:
                 sweep(args)
+            return
+        if args.op:
+            if dist.rank == 0:
+                single_op(args)
             return
         import fp8_token_group_bf16_b300 as fq
 
