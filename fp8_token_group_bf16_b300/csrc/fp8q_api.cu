@@ -14,6 +14,10 @@ namespace {
 
 using namespace fp8q;
 
+#ifndef FP8Q_ROPE_LANES
+#define FP8Q_ROPE_LANES 4
+#endif
+
 static_assert(FP8Q_TOKEN_MAX_COLS == kTokenMaxGroups * kGroup, "per-token row limit");
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -403,12 +407,13 @@ int fp8q_fused_qk_norm_rope(void *qkv, const void *q_weight, const void *k_weigh
     auto qw = static_cast<const uint16_t *>(q_weight);
     auto kw = static_cast<const uint16_t *>(k_weight);
     auto cs = static_cast<const uint16_t *>(cos_sin);
-    const dim3 grid{unsigned((n + 63) / 64)}, block{256};
+    constexpr int kLph = FP8Q_ROPE_LANES;   // lanes per head
+    const dim3 grid{unsigned((n + 256 / kLph - 1) / (256 / kLph))}, block{256};
     auto st = static_cast<cudaStream_t>(stream);
     const int nhi = int(nh), hq = int(num_q_heads);
     cudaError_t e;
-#define FP8Q_ROPE(N, V) launch(qk_norm_rope_kernel<N, V>, grid, block, st, x, qw, kw, cs, positions, n, nhi, hq, row, \
-                               max_position, eps)
+#define FP8Q_ROPE(N, V) launch(qk_norm_rope_kernel<kLph, N, V>, grid, block, st, x, qw, kw, cs, positions, n, nhi, hq, \
+                               row, max_position, eps)
     if (is_neox)
         e = v8 ? FP8Q_ROPE(true, true) : FP8Q_ROPE(true, false);
     else

@@ -21,14 +21,16 @@ namespace fp8q {
 
 constexpr int kRmsMaxThreads = 256;
 
-// Squares of one lane's 32 values (16 bf16x2 words), summed exactly:
-// returns (hi, lo) with hi + lo equal to the sum up to lo's own rounding.
-// The two halves of the packed pair accumulate the even and the odd values.
-__device__ __forceinline__ void lane_sumsq(const uint32_t (&w)[16], float &hi, float &lo)
+// Squares of one lane's 2*NW values (NW bf16x2 words, NW even), summed
+// exactly: returns (hi, lo) with hi + lo equal to the sum up to lo's own
+// rounding.  The two halves of the packed pair accumulate the even and the
+// odd values.
+template <int NW>
+__device__ __forceinline__ void lane_sumsq(const uint32_t (&w)[NW], float &hi, float &lo)
 {
     float m0 = 0.0f, m1 = 0.0f;
 #pragma unroll
-    for (int k = 0; k < 16; k += 2) {
+    for (int k = 0; k < NW; k += 2) {
         m0 = absmax3(m0, bf_lo(w[k]), bf_hi(w[k]));
         m1 = absmax3(m1, bf_lo(w[k + 1]), bf_hi(w[k + 1]));
     }
@@ -37,7 +39,7 @@ __device__ __forceinline__ void lane_sumsq(const uint32_t (&w)[16], float &hi, f
     uint64_t s = f2_pack(pm, pm);
     uint64_t c = f2_pack(0.0f, 0.0f);
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
+    for (int k = 0; k < NW; ++k) {
         const uint64_t z = f2_from_bf16x2(w[k]);
         const uint64_t p = f2_mul(z, z);
         const uint64_t t = f2_add(s, p);

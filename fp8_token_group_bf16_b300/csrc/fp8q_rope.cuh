@@ -76,12 +76,44 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi)
     return r;
 }
 
-// Grid: one quad per (token, head) unit over the T * (Hq + Hkv) query and key
-// heads, flat (unit u: token u / nh, head u % nh, nh = Hq + Hkv); 64 units
-// per CTA of 256 threads.  Positions outside [0, P) are clamped into the
-// table (the result for such a token is unspecified, the access stays in
-// bounds).
-template <bool NEOX, bool V8>
+// `piece` bf16 values (16 or 8) that this kernel also writes: coherent path.
+template <int NWP, bool V8>
+__device__ __forceinline__ void ld_piece_rw(const uint16_t *p, uint32_t *w)
+{
+    if (NWP == 8)
+        ld32_rw<V8>(p, w);
+    else
+        FP8Q_LD4(".L1::no_allocate", p, w[0], w[1], w[2], w[3]);
+}
+
+template <int NWP, bool V8>
+__device__ __forceinline__ void ld_piece_table(const uint16_t *p, uint32_t *w)
+{
+    if (NWP == 8)
+        ld32_table<V8>(p, w);
+    else
+        FP8Q_LD4(".nc", p, w[0], w[1], w[2], w[3]);
+}
+
+template <int NWP, bool V8>
+__device__ __forceinline__ void st_piece(uint16_t *p, const uint32_t *w)
+{
+    if (NWP == 8)
+        st32_words<V8>(p, w);
+    else
+        asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                     : "memory");
+}
+
+// Grid: LPH lanes (4 or 8) per (token, head) unit over the T * (Hq + Hkv)
+// query and key heads, flat (unit u: token u / nh, head u % nh,
+// nh = Hq + Hkv); 256 / LPH units per CTA of 256 threads.  A lane holds
+// 128 / LPH values as two pieces of 64 / LPH: neox, dims piece*s.. and
+// 64 + piece*s..; interleaved, dims 2*piece*s.. and the next piece.  Either
+// way it uses cos/sin entries j = piece*s .. piece*s + piece - 1.
+// Positions outside [0, P) are clamped into the table (the result for such
+// a token is unspecified, the access stays in bounds).
+template <int LPH, bool NEOX, bool V8>
 __global__ void __launch_bounds__(256) qk_norm_rope_kernel(uint16_t *__restrict__ qkv,
                                                            const uint16_t *__restrict__ q_w,
                                                            const uint16_t *__restrict__ k_w,
@@ -89,53 +121,56 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(uint16_t *__restrict_
                                                            const int64_t *__restrict__ positions, int64_t n_units,
                                                            int nh, int Hq, int64_t row, int64_t P, float eps)
 {
-    const int sub = threadIdx.x & 3;
-    const int64_t u = int64_t(blockIdx.x) * 64 + (threadIdx.x >> 2);
+    constexpr int VPL = kHeadDim / LPH;   // values per lane
+    constexpr int NW = VPL / 2;            // bf16x2 words per lane
+    constexpr int NWP = NW / 2;            // words per piece
+    constexpr int PIECE = VPL / 2;         // values per piece
+    const int sub = threadIdx.x & (LPH - 1);
+    const int64_t u = int64_t(blockIdx.x) * (256 / LPH) + (threadIdx.x / LPH);
     const int64_t ul = u < n_units ? u : n_units - 1;
     const uint32_t t = uint32_t(ul) / uint32_t(nh), h = uint32_t(ul) - t * uint32_t(nh);
     uint16_t *xh = qkv + int64_t(t) * row + int64_t(h) * kHeadDim;
     const uint16_t *w = h < uint32_t(Hq) ? q_w : k_w;
-    // element offsets of the lane's two 16-value pieces
-    const int o0 = NEOX ? 16 * sub : 32 * sub;
-    const int o1 = NEOX ? 64 + 16 * sub : 32 * sub + 16;
+    const int o0 = NEOX ? PIECE * sub : VPL * sub;
+    const int o1 = NEOX ? kHeadDim / 2 + PIECE * sub : VPL * sub + PIECE;
 
     wait_for_producer();
     allow_consumer_launch();
 
-    uint32_t z[16], wr[16], cs[16];
-    ld32_rw<V8>(xh + o0, z);
-    ld32_rw<V8>(xh + o1, z + 8);
+    uint32_t z[NW], wr[NW], cs[NW];
+    ld_piece_rw<NWP, V8>(xh + o0, z);
+    ld_piece_rw<NWP, V8>(xh + o1, z + NWP);
     int64_t pos = positions[t];
     pos = pos < 0 ? 0 : (pos >= P ? P - 1 : pos);
     const uint16_t *crow = cos_sin + pos * kHeadDim;
-    ld32_table<V8>(w + o0, wr);
-    ld32_table<V8>(w + o1, wr + 8);
-    ld32_table<V8>(crow + 16 * sub, cs);            // cos_j, j = 16 sub ..
-    ld32_table<V8>(crow + 64 + 16 * sub, cs + 8);   // sin_j
+    ld_piece_table<NWP, V8>(w + o0, wr);
+    ld_piece_table<NWP, V8>(w + o1, wr + NWP);
+    ld_piece_table<NWP, V8>(crow + PIECE * sub, cs);                   // cos_j
+    ld_piece_table<NWP, V8>(crow + kHeadDim / 2 + PIECE * sub, cs + NWP);   // sin_j
 
-    // ---- 1/rms of the head: exact lane sums, TwoSum across the quad
+    // ---- 1/rms of the head: exact lane sums, TwoSum across the head's lanes
     float hi, lo;
     lane_sumsq(z, hi, lo);
 #pragma unroll
-    for (int o = 1; o <= 2; o <<= 1)
+    for (int o = 1; o < LPH; o <<= 1)
         pair_add(hi, lo, __shfl_xor_sync(0xFFFFFFFFu, hi, o), __shfl_xor_sync(0xFFFFFFFFu, lo, o));
     const float inv = rms_inv(hi, lo, kHeadDim, eps);
     const uint64_t inv2 = f2_pack(inv, inv);
 
     // ---- y = (z * inv) * w, then the rotation of each (a, b) pair
-    uint32_t out[16];
+    uint32_t out[NW];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        // table word k holds cos (or sin) of j = 16 sub + 2k and 2k + 1
-        const uint64_t c = f2_from_bf16x2(cs[k]), s = f2_from_bf16x2(cs[8 + k]);
+    for (int k = 0; k < NWP; ++k) {
+        // table word k holds cos (or sin) of j = PIECE sub + 2k and 2k + 1
+        const uint64_t c = f2_from_bf16x2(cs[k]), s = f2_from_bf16x2(cs[NWP + k]);
         uint64_t a, b;
         if (NEOX) {
-            // z word k: dims 16 sub + 2k, +1 (first half); word 8 + k: the partners
+            // z word k: dims PIECE sub + 2k, +1 (first half); word NWP + k: the partners
             a = f2_mul(f2_mul(f2_from_bf16x2(z[k]), inv2), f2_from_bf16x2(wr[k]));
-            b = f2_mul(f2_mul(f2_from_bf16x2(z[8 + k]), inv2), f2_from_bf16x2(wr[8 + k]));
+            b = f2_mul(f2_mul(f2_from_bf16x2(z[NWP + k]), inv2), f2_from_bf16x2(wr[NWP + k]));
         } else {
-            // z word m holds dims 32 sub + 2m, +1: the pair j = 16 sub + m; words
-            // 2k, 2k+1 are the pairs j = 16 sub + 2k and j + 1, (a0, b0), (a1, b1)
+            // z word m holds dims VPL sub + 2m, +1: the pair j = PIECE sub + m; words
+            // 2k, 2k+1 are the pairs j = PIECE sub + 2k and j + 1, (a0, b0), (a1, b1)
             const int k0 = 2 * k;
             const uint64_t y0 = f2_mul(f2_mul(f2_from_bf16x2(z[k0]), inv2), f2_from_bf16x2(wr[k0]));
             const uint64_t y1 = f2_mul(f2_mul(f2_from_bf16x2(z[k0 + 1]), inv2), f2_from_bf16x2(wr[k0 + 1]));
@@ -160,15 +195,15 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(uint16_t *__restrict_
         const float b1 = __fadd_rn(__fmul_rn(yb1, c1), __fmul_rn(ya1, s1));
         if (NEOX) {
             out[k] = bf16x2_rn(a0, a1);
-            out[8 + k] = bf16x2_rn(b0, b1);
+            out[NWP + k] = bf16x2_rn(b0, b1);
         } else {
             out[2 * k] = bf16x2_rn(a0, b0);
             out[2 * k + 1] = bf16x2_rn(a1, b1);
         }
     }
     if (u < n_units) {
-        st32_words<V8>(xh + o0, out);
-        st32_words<V8>(xh + o1, out + 8);
+        st_piece<NWP, V8>(xh + o0, out);
+        st_piece<NWP, V8>(xh + o1, out + NWP);
     }
 }
 
