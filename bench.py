@@ -439,50 +439,94 @@ def time_device(step: DeviceStep, steps: int, warmup: int, dist: Dist):
     return total_ms / 1e3, {op: sum(v) / len(v) for op, v in per_op.items()}, (t0, t1)
 
 
-def time_e2e(host, steps: int, dist: Dist):
+def time_e2e(host, steps: int, dist: Dist, chunks: int = 8):
     """Public tensor API from pinned host memory: per step copy the three
-    inputs in, run the three ops, copy every output (codes and scales) out."""
+    inputs in, run the three ops, copy every output (codes and scales) out.
+
+    The host link, not the kernels, bounds this number, so a step is
+    pipelined over `chunks` token slices on three streams: slice i's inputs
+    go in on the copy-in stream while slice i-1 is computed and slice i-2's
+    outputs go out on the copy-out stream (the link carries both directions
+    at once).  Rows are independent in all three ops, so a slice is a
+    complete call of each op on its rows; op A's column-major scales come back
+    per slice ([G, rows of the slice] each)."""
     import torch
 
     import fp8_token_group_bf16_b300 as fq
 
     dev = torch.device("cuda", torch.cuda.current_device())
     pinned = {op: tuple(t.pin_memory() for t in ts) for op, ts in host.items()}
-    xa_d = torch.empty_like(pinned["per_token_group_fp8_quant"][0], device=dev)
-    xb_d = torch.empty_like(pinned["rms_norm_per_block_quant"][0], device=dev)
-    wb_d = torch.empty_like(pinned["rms_norm_per_block_quant"][1], device=dev)
-    xc_d = torch.empty_like(pinned["silu_and_mul_per_block_quant"][0], device=dev)
-    T = xa_d.shape[0]
-    h2d = sum(t.numel() * t.element_size() for ts in pinned.values() for t in ts)
+    xa_h = pinned["per_token_group_fp8_quant"][0]
+    xb_h, wb_h = pinned["rms_norm_per_block_quant"][:2]
+    xc_h = pinned["silu_and_mul_per_block_quant"][0]
+    T = xa_h.shape[0]
+    chunks = max(1, min(chunks, T))
+    bounds = [(T * i // chunks, T * (i + 1) // chunks) for i in range(chunks)]
+    xa_d, xb_d, xc_d = (torch.empty_like(t, device=dev) for t in (xa_h, xb_h, xc_h))
+    wb_d = torch.empty_like(wb_h, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in (xa_h, xb_h, wb_h, xc_h))
+    s_in, s_c, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    outs_dev, outs_host = [], []
+    for lo, hi in bounds:   # per-slice output buffers, device and pinned host
+        n = hi - lo
+        shapes = [((n, xa_h.shape[1]), torch.float8_e4m3fn), ((xa_h.shape[1] // 128, n), torch.float32),
+                  ((n, xb_h.shape[1]), torch.float8_e4m3fn), ((n, xb_h.shape[1] // 128), torch.float32),
+                  ((n, xc_h.shape[1] // 2), torch.float8_e4m3fn), ((n, xc_h.shape[1] // 256), torch.float32)]
+        outs_dev.append([torch.empty(sh, dtype=dt, device=dev) for sh, dt in shapes])
+        outs_host.append([torch.empty(sh, dtype=dt, pin_memory=True) for sh, dt in shapes])
+    d2h = sum(o.numel() * o.element_size() for os_ in outs_dev for o in os_)
+
+    prev = {"c_done": None, "out": [None] * len(bounds)}
 
     def one_step():
-        xa_d.copy_(pinned["per_token_group_fp8_quant"][0], non_blocking=True)
-        xb_d.copy_(pinned["rms_norm_per_block_quant"][0], non_blocking=True)
-        wb_d.copy_(pinned["rms_norm_per_block_quant"][1], non_blocking=True)
-        xc_d.copy_(pinned["silu_and_mul_per_block_quant"][0], non_blocking=True)
-        a = fq.per_token_group_fp8_quant(xa_d, ue8m0=True, column_major_scales=True)
-        b = fq.rms_norm_per_block_quant(xb_d, wb_d, ue8m0=True)
-        c = fq.silu_and_mul_per_block_quant(xc_d, ue8m0=True)
-        # column-major scales are a transposed view of a contiguous [G, T]
-        # buffer: copy that buffer as it is (no device-side reshuffle)
-        return [o if o.is_contiguous() else o.t() for pair in (a, b, c) for o in pair]
+        # the previous step's readers of the buffers this step overwrites
+        # (its compute of the inputs, its copy-out of the output slices) come first
+        ev_in = [torch.cuda.Event() for _ in bounds]
+        ev_c = [torch.cuda.Event() for _ in bounds]
+        ev_out = [torch.cuda.Event() for _ in bounds]
+        with torch.cuda.stream(s_in):
+            if prev["c_done"] is not None:
+                s_in.wait_event(prev["c_done"])
+            wb_d.copy_(wb_h, non_blocking=True)
+            for i, (lo, hi) in enumerate(bounds):
+                xa_d[lo:hi].copy_(xa_h[lo:hi], non_blocking=True)
+                xb_d[lo:hi].copy_(xb_h[lo:hi], non_blocking=True)
+                xc_d[lo:hi].copy_(xc_h[lo:hi], non_blocking=True)
+                ev_in[i].record(s_in)
+        for i, (lo, hi) in enumerate(bounds):
+            s_c.wait_event(ev_in[i])
+            if prev["out"][i] is not None:
+                s_c.wait_event(prev["out"][i])
+            qa, sa, qb, sb, qc, sc = outs_dev[i]
+            fq.per_token_group_fp8_quant(xa_d[lo:hi], ue8m0=True, column_major_scales=True, q=qa, scales=sa.t(),
+                                         stream=s_c)
+            fq.rms_norm_per_block_quant(xb_d[lo:hi], wb_d, ue8m0=True, q=qb, scales=sb, stream=s_c)
+            fq.silu_and_mul_per_block_quant(xc_d[lo:hi], ue8m0=True, q=qc, scales=sc, stream=s_c)
+            ev_c[i].record(s_c)
+        c_done = torch.cuda.Event()
+        c_done.record(s_c)
+        with torch.cuda.stream(s_out):
+            for i in range(len(bounds)):
+                s_out.wait_event(ev_c[i])
+                for o, h in zip(outs_dev[i], outs_host[i]):
+                    h.copy_(o, non_blocking=True)
+                ev_out[i].record(s_out)
+        prev["c_done"], prev["out"] = c_done, ev_out
 
-    outs = one_step()
-    outs_host = [torch.empty(o.shape, dtype=o.dtype, device="cpu", pin_memory=True) for o in outs]
-    d2h = sum(o.numel() * o.element_size() for o in outs)
+    one_step()
     torch.cuda.synchronize()
     dist.barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(steps):
-        for o, h in zip(one_step(), outs_host):
-            h.copy_(o, non_blocking=True)
+        one_step()
     torch.cuda.synchronize()
     secs = time.perf_counter() - t0
     dist.barrier()
     agg = aggregate(step_bytes(T) * steps, secs, dist, steps)
     return {"value": round(agg["value"], 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(agg["ms_per_step"], 3)}
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(agg["ms_per_step"], 3),
+            "pipeline": f"{chunks} token slices, copy-in / compute / copy-out streams"}
 
 
 # ------------------------------------------------------------ CPU oracle ---
