@@ -151,3 +151,95 @@ def test_graph_replay_matches_oracle():
         torch.cuda.synchronize()
         qr, sr, _ = oracle.per_token_group_quant(xb)
         assert_exact(q.view(torch.uint8).cpu().numpy(), s.cpu().numpy(), qr, sr, f"graph seed={seed}")
+
+
+@pytest.mark.parametrize("T,H", [(1, 128), (5, 640), (37, 896), (130, 8320)])
+@pytest.mark.parametrize("op", ["group", "rms", "silu"])
+def test_packed_scales_no_writes_outside(T, H, op):
+    """Packed UE8M0 scales: exactly the packed bytes are written (padding
+    included), nothing around them."""
+    xb = inputs.bits(inputs.heavy_tailed_input(T, 2 * H if op == "silu" else H, seed=T + 7 * H))
+    x = dev_bf16(xb)
+    G = H // 128
+    nbytes = -(-G // 4) * (-(-T // 4) * 4) * 4
+    qraw, q = _guarded(T * H)
+    sraw, s = _guarded(nbytes, torch.int32)
+    P, st = fq.FP8Q_SCALES_UE8M0_PACKED, _stream()
+    if op == "group":
+        rc = fq.fp8q_per_token_group_quant(x.data_ptr(), q.data_ptr(), s.data_ptr(), T, H, 128, 1e-10, 1, P, st)
+    elif op == "silu":
+        rc = fq.fp8q_silu_and_mul_per_block_quant(x.data_ptr(), q.data_ptr(), s.data_ptr(), T, H, 128, 1e-10, 1,
+                                                  P, st)
+    else:
+        w = dev_bf16(inputs.bits(inputs.rms_weight(H)))
+        rc = fq.fp8q_rms_norm_per_block_quant(x.data_ptr(), None, w.data_ptr(), q.data_ptr(), s.data_ptr(), T, H,
+                                              128, 1e-6, 1, P, st)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert _canaries_intact(qraw, T * H) and _canaries_intact(sraw, nbytes)
+    assert not bool((s.view(torch.uint8) == 0xA5).any()), "every packed byte is written"
+
+
+@pytest.mark.parametrize("T,H", [(1, 128), (3, 896), (7, 8320), (2, 65536)])
+@pytest.mark.parametrize("op", ["token", "token_silu", "token_rms"])
+def test_per_token_no_writes_outside(T, H, op):
+    if op == "token_rms" and H > fq.FP8Q_RMS_MAX_H:
+        pytest.skip("longer than the RMSNorm row limit")
+    xb = inputs.bits(inputs.heavy_tailed_input(T, 2 * H if op == "token_silu" else H, seed=T + 11 * H))
+    x = dev_bf16(xb)
+    qraw, q = _guarded(T * H)
+    sraw, s = _guarded(T * 4, torch.float32)
+    st = _stream()
+    if op == "token":
+        rc = fq.fp8q_dynamic_per_token_scaled_fp8_quant(x.data_ptr(), q.data_ptr(), s.data_ptr(), T, H, 1e-10, 0, st)
+    elif op == "token_silu":
+        rc = fq.fp8q_silu_and_mul_dynamic_per_token_quant(x.data_ptr(), q.data_ptr(), s.data_ptr(), T, H, 1e-10, 1,
+                                                          st)
+    else:
+        w = dev_bf16(inputs.bits(inputs.rms_weight(H)))
+        rc = fq.fp8q_rms_norm_dynamic_per_token_quant(x.data_ptr(), None, w.data_ptr(), q.data_ptr(), s.data_ptr(),
+                                                      T, H, 1e-6, 0, st)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert _canaries_intact(qraw, T * H) and _canaries_intact(sraw, T * 4)
+
+
+def test_qk_norm_rope_no_writes_outside():
+    T, Hq, Hkv = 9, 8, 2
+    qkv, qw, kw, cs, pos = inputs.qk_norm_rope_input(T, Hq, Hkv, P=64, seed=31)
+    n = qkv.numel() * 2
+    raw, buf = _guarded(n, torch.bfloat16)
+    x = buf.view(qkv.shape)
+    x.copy_(qkv.cuda())
+    fq.fused_qk_norm_rope(x, qw.cuda(), kw.cuda(), cs.cuda(), pos.cuda(), Hq, Hkv)
+    torch.cuda.synchronize()
+    assert _canaries_intact(raw, n)
+
+
+def test_widened_ops_in_a_graph():
+    """Packed scales, the per-token ops (a clustered launch) and the rotary
+    kernel captured in one CUDA graph give the eager results."""
+    xa = dev_bf16(inputs.bits(inputs.heavy_tailed_input(64, 25600, seed=41)))
+    xs = dev_bf16(inputs.bits(inputs.silu_input(64, 25600, seed=42)))
+    qkv, qw, kw, cs, pos = [t.cuda() for t in inputs.qk_norm_rope_input(32, 16, 4, P=256, seed=43)]
+
+    def run(qkv_buf):
+        a = fq.per_token_group_fp8_quant(xa, ue8m0=True, packed_ue8m0_scales=True)
+        b = fq.dynamic_per_token_scaled_fp8_quant(xa)
+        c = fq.silu_and_mul_dynamic_per_token_quant(xs, ue8m0=True)
+        fq.fused_qk_norm_rope(qkv_buf, qw, kw, cs, pos, 16, 4)
+        return (*a, *b, *c, qkv_buf)
+
+    eager = run(qkv.clone())
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    static_qkv = qkv.clone()
+    with torch.cuda.graph(g):
+        captured = run(static_qkv)
+    static_qkv.copy_(qkv)
+    g.replay()
+    torch.cuda.synchronize()
+    for e, o in zip(eager, captured):
+        e8 = e.view(torch.uint8) if e.dtype == torch.float8_e4m3fn else e
+        o8 = o.view(torch.uint8) if o.dtype == torch.float8_e4m3fn else o
+        assert torch.equal(e8, o8)
