@@ -439,94 +439,105 @@ def time_device(step: DeviceStep, steps: int, warmup: int, dist: Dist):
     return total_ms / 1e3, {op: sum(v) / len(v) for op, v in per_op.items()}, (t0, t1)
 
 
-def time_e2e(host, steps: int, dist: Dist, chunks: int = 8):
-    """Public tensor API from pinned host memory: per step copy the three
-    inputs in, run the three ops, copy every output (codes and scales) out.
+class E2EPipeline:
+    """One end-to-end step through the public tensor API from pinned host
+    memory: copy the three inputs in, run the three ops, copy every output
+    (codes and scales) out.
 
-    The host link, not the kernels, bounds this number, so a step is
-    pipelined over `chunks` token slices on three streams: slice i's inputs
-    go in on the copy-in stream while slice i-1 is computed and slice i-2's
-    outputs go out on the copy-out stream (the link carries both directions
-    at once).  Rows are independent in all three ops, so a slice is a
-    complete call of each op on its rows; op A's column-major scales come back
-    per slice ([G, rows of the slice] each)."""
-    import torch
+    The host link, not the kernels, bounds this, so a step is pipelined over
+    `chunks` token slices on three streams: slice i's inputs go in on the
+    copy-in stream while slice i-1 is computed and slice i-2's outputs go out
+    on the copy-out stream.  Rows are independent in all three ops, so a slice
+    is a complete call of each op on its rows; op A's column-major scales
+    come back per slice ([G, rows of the slice] each).  Each step waits for
+    the previous step's readers of the buffers it overwrites."""
 
-    import fp8_token_group_bf16_b300 as fq
+    def __init__(self, host, chunks: int = 8):
+        import torch
 
-    dev = torch.device("cuda", torch.cuda.current_device())
-    pinned = {op: tuple(t.pin_memory() for t in ts) for op, ts in host.items()}
-    xa_h = pinned["per_token_group_fp8_quant"][0]
-    xb_h, wb_h = pinned["rms_norm_per_block_quant"][:2]
-    xc_h = pinned["silu_and_mul_per_block_quant"][0]
-    T = xa_h.shape[0]
-    chunks = max(1, min(chunks, T))
-    bounds = [(T * i // chunks, T * (i + 1) // chunks) for i in range(chunks)]
-    xa_d, xb_d, xc_d = (torch.empty_like(t, device=dev) for t in (xa_h, xb_h, xc_h))
-    wb_d = torch.empty_like(wb_h, device=dev)
-    h2d = sum(t.numel() * t.element_size() for t in (xa_h, xb_h, wb_h, xc_h))
-    s_in, s_c, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    outs_dev, outs_host = [], []
-    for lo, hi in bounds:   # per-slice output buffers, device and pinned host
-        n = hi - lo
-        shapes = [((n, xa_h.shape[1]), torch.float8_e4m3fn), ((xa_h.shape[1] // 128, n), torch.float32),
-                  ((n, xb_h.shape[1]), torch.float8_e4m3fn), ((n, xb_h.shape[1] // 128), torch.float32),
-                  ((n, xc_h.shape[1] // 2), torch.float8_e4m3fn), ((n, xc_h.shape[1] // 256), torch.float32)]
-        outs_dev.append([torch.empty(sh, dtype=dt, device=dev) for sh, dt in shapes])
-        outs_host.append([torch.empty(sh, dtype=dt, pin_memory=True) for sh, dt in shapes])
-    d2h = sum(o.numel() * o.element_size() for os_ in outs_dev for o in os_)
+        self.torch = torch
+        dev = torch.device("cuda", torch.cuda.current_device())
+        pinned = {op: tuple(t.pin_memory() for t in ts) for op, ts in host.items()}
+        self.xa_h = pinned["per_token_group_fp8_quant"][0]
+        self.xb_h, self.wb_h = pinned["rms_norm_per_block_quant"][:2]
+        self.xc_h = pinned["silu_and_mul_per_block_quant"][0]
+        T = self.T = self.xa_h.shape[0]
+        chunks = max(1, min(chunks, T))
+        self.bounds = [(T * i // chunks, T * (i + 1) // chunks) for i in range(chunks)]
+        self.xa_d, self.xb_d, self.xc_d = (torch.empty_like(t, device=dev) for t in (self.xa_h, self.xb_h, self.xc_h))
+        self.wb_d = torch.empty_like(self.wb_h, device=dev)
+        self.h2d = sum(t.numel() * t.element_size() for t in (self.xa_h, self.xb_h, self.wb_h, self.xc_h))
+        self.streams = [torch.cuda.Stream() for _ in range(3)]
+        self.outs_dev, self.outs_host = [], []
+        ha, hb, hc = self.xa_h.shape[1], self.xb_h.shape[1], self.xc_h.shape[1] // 2
+        for lo, hi in self.bounds:   # per-slice output buffers, device and pinned host
+            n = hi - lo
+            shapes = [((n, ha), torch.float8_e4m3fn), ((ha // 128, n), torch.float32),
+                      ((n, hb), torch.float8_e4m3fn), ((n, hb // 128), torch.float32),
+                      ((n, hc), torch.float8_e4m3fn), ((n, hc // 128), torch.float32)]
+            self.outs_dev.append([torch.empty(sh, dtype=dt, device=dev) for sh, dt in shapes])
+            self.outs_host.append([torch.empty(sh, dtype=dt, pin_memory=True) for sh, dt in shapes])
+        self.d2h = sum(o.numel() * o.element_size() for os_ in self.outs_dev for o in os_)
+        self.prev_c_done, self.prev_out = None, [None] * len(self.bounds)
 
-    prev = {"c_done": None, "out": [None] * len(bounds)}
+    def step(self):
+        import fp8_token_group_bf16_b300 as fq
 
-    def one_step():
-        # the previous step's readers of the buffers this step overwrites
-        # (its compute of the inputs, its copy-out of the output slices) come first
-        ev_in = [torch.cuda.Event() for _ in bounds]
-        ev_c = [torch.cuda.Event() for _ in bounds]
-        ev_out = [torch.cuda.Event() for _ in bounds]
+        torch = self.torch
+        s_in, s_c, s_out = self.streams
+        ev_in = [torch.cuda.Event() for _ in self.bounds]
+        ev_c = [torch.cuda.Event() for _ in self.bounds]
+        ev_out = [torch.cuda.Event() for _ in self.bounds]
         with torch.cuda.stream(s_in):
-            if prev["c_done"] is not None:
-                s_in.wait_event(prev["c_done"])
-            wb_d.copy_(wb_h, non_blocking=True)
-            for i, (lo, hi) in enumerate(bounds):
-                xa_d[lo:hi].copy_(xa_h[lo:hi], non_blocking=True)
-                xb_d[lo:hi].copy_(xb_h[lo:hi], non_blocking=True)
-                xc_d[lo:hi].copy_(xc_h[lo:hi], non_blocking=True)
+            if self.prev_c_done is not None:
+                s_in.wait_event(self.prev_c_done)
+            self.wb_d.copy_(self.wb_h, non_blocking=True)
+            for i, (lo, hi) in enumerate(self.bounds):
+                self.xa_d[lo:hi].copy_(self.xa_h[lo:hi], non_blocking=True)
+                self.xb_d[lo:hi].copy_(self.xb_h[lo:hi], non_blocking=True)
+                self.xc_d[lo:hi].copy_(self.xc_h[lo:hi], non_blocking=True)
                 ev_in[i].record(s_in)
-        for i, (lo, hi) in enumerate(bounds):
+        for i, (lo, hi) in enumerate(self.bounds):
             s_c.wait_event(ev_in[i])
-            if prev["out"][i] is not None:
-                s_c.wait_event(prev["out"][i])
-            qa, sa, qb, sb, qc, sc = outs_dev[i]
-            fq.per_token_group_fp8_quant(xa_d[lo:hi], ue8m0=True, column_major_scales=True, q=qa, scales=sa.t(),
-                                         stream=s_c)
-            fq.rms_norm_per_block_quant(xb_d[lo:hi], wb_d, ue8m0=True, q=qb, scales=sb, stream=s_c)
-            fq.silu_and_mul_per_block_quant(xc_d[lo:hi], ue8m0=True, q=qc, scales=sc, stream=s_c)
+            if self.prev_out[i] is not None:
+                s_c.wait_event(self.prev_out[i])
+            qa, sa, qb, sb, qc, sc = self.outs_dev[i]
+            fq.per_token_group_fp8_quant(self.xa_d[lo:hi], ue8m0=True, column_major_scales=True, q=qa,
+                                         scales=sa.t(), stream=s_c)
+            fq.rms_norm_per_block_quant(self.xb_d[lo:hi], self.wb_d, ue8m0=True, q=qb, scales=sb, stream=s_c)
+            fq.silu_and_mul_per_block_quant(self.xc_d[lo:hi], ue8m0=True, q=qc, scales=sc, stream=s_c)
             ev_c[i].record(s_c)
         c_done = torch.cuda.Event()
         c_done.record(s_c)
         with torch.cuda.stream(s_out):
-            for i in range(len(bounds)):
+            for i in range(len(self.bounds)):
                 s_out.wait_event(ev_c[i])
-                for o, h in zip(outs_dev[i], outs_host[i]):
+                for o, h in zip(self.outs_dev[i], self.outs_host[i]):
                     h.copy_(o, non_blocking=True)
                 ev_out[i].record(s_out)
-        prev["c_done"], prev["out"] = c_done, ev_out
+        self.prev_c_done, self.prev_out = c_done, ev_out
 
-    one_step()
+
+def time_e2e(host, steps: int, dist: Dist, chunks: int = 8):
+    """The end-to-end metric: `steps` pipelined steps (E2EPipeline) between
+    two synchronisations, host wall clock, max over ranks."""
+    import torch
+
+    pipe = E2EPipeline(host, chunks)
+    pipe.step()
     torch.cuda.synchronize()
     dist.barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(steps):
-        one_step()
+        pipe.step()
     torch.cuda.synchronize()
     secs = time.perf_counter() - t0
     dist.barrier()
-    agg = aggregate(step_bytes(T) * steps, secs, dist, steps)
-    return {"value": round(agg["value"], 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(agg["ms_per_step"], 3),
-            "pipeline": f"{chunks} token slices, copy-in / compute / copy-out streams"}
+    agg = aggregate(step_bytes(pipe.T) * steps, secs, dist, steps)
+    return {"value": round(agg["value"], 2), "unit": UNIT, "h2d_bytes_per_step": pipe.h2d,
+            "d2h_bytes_per_step": pipe.d2h, "steps": steps, "ms_per_step": round(agg["ms_per_step"], 3),
+            "pipeline": f"{len(pipe.bounds)} token slices, copy-in / compute / copy-out streams"}
 
 
 # ------------------------------------------------------------ CPU oracle ---
