@@ -165,6 +165,9 @@ def aggregate(bytes_per_rank: float, seconds_per_rank: float, dist: Dist, steps:
 # ----------------------------------------------------------------- peaks ---
 
 
+NOMINAL_HBM_GBS = 7700.0   # B300 HBM3e, nominal
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -658,10 +661,13 @@ def sweep(args):
         return statistics.median(ts) * 1e3
 
     def copy_maker(nbytes):
+        # an SM-side copy (elementwise x * 1 on fp32 words): a plain D2D memcpy
+        # may be handed to a copy engine, which is slower at some sizes
         def make():
-            a = torch.empty(nbytes // 2, dtype=torch.uint8, device=dev)
-            b = torch.empty(nbytes // 2, dtype=torch.uint8, device=dev)
-            return lambda: b.copy_(a)
+            n = max(1, nbytes // 8)
+            a = torch.zeros(n, dtype=torch.float32, device=dev)
+            b = torch.empty(n, dtype=torch.float32, device=dev)
+            return lambda: torch.mul(a, 1.0, out=b)
         return make
 
     e4 = torch.float8_e4m3fn
@@ -719,7 +725,8 @@ def sweep(args):
         torch.cuda.empty_cache()
         row = {"op": op, "T": T, "H_or_I": H, "ue8m0": ue8m0, "scales": lay, "residual": res,
                "bytes": nbytes, "us": round(us, 3), "GBps": round(nbytes / us / 1e3, 1),
-               "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "copy_us": round(cus, 3),
+               "frac_of_peak": round(nbytes / us / 1e3 / peak, 4),
+               "frac_of_nominal": round(nbytes / us / 1e3 / NOMINAL_HBM_GBS, 4), "copy_us": round(cus, 3),
                "copy_GBps": round(nbytes / cus / 1e3, 1), "peak": peak, "peak_kind": peak_kind}
         rows.append(row)
         print(json.dumps(row), flush=True)
@@ -743,7 +750,8 @@ def sweep(args):
         torch.cuda.empty_cache()
         row = {"op": "fused_qk_norm_rope", "T": T, "H_or_I": "64q+8kv x 128", "ue8m0": None, "scales": None,
                "residual": False, "bytes": nbytes, "us": round(us, 3), "GBps": round(nbytes / us / 1e3, 1),
-               "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "copy_us": round(cus, 3),
+               "frac_of_peak": round(nbytes / us / 1e3 / peak, 4),
+               "frac_of_nominal": round(nbytes / us / 1e3 / NOMINAL_HBM_GBS, 4), "copy_us": round(cus, 3),
                "copy_GBps": round(nbytes / cus / 1e3, 1), "peak": peak, "peak_kind": peak_kind}
         rows.append(row)
         print(json.dumps(row), flush=True)
@@ -899,7 +907,8 @@ def main(argv=None):
                          "peak_source": (f"{peak_kind}: MEASURED_PEAKS.json hbm_gbs (device copy bandwidth)"
                                          if peak_kind == "measured" else "fallback 6.4 TB/s"),
                          "traffic": traffic,
-                         "algorithmic_bytes_per_launch": step.bytes[DOMINANT]},
+                         "algorithmic_bytes_per_launch": step.bytes[DOMINANT],
+                         "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4)},
             "ops": {op: {"us_per_launch": round(ms * 1e3, 2),
                          "GBps": round(step.bytes[op] / (ms * 1e-3) / 1e9, 1),
                          "frac_of_peak": round(step.bytes[op] / (ms * 1e-3) / 1e9 / peak, 4),
