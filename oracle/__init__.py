@@ -104,6 +104,8 @@ def _configure(L: ctypes.CDLL) -> ctypes.CDLL:
     L.oracle_fused_qk_norm_rope.restype = I
     L.oracle_pack_ue8m0.argtypes = [P, I64, I64, P]
     L.oracle_pack_ue8m0.restype = I
+    L.oracle_pack_ue8m0_mx.argtypes = [P, I64, I64, P]
+    L.oracle_pack_ue8m0_mx.restype = I
     L.oracle_f32_to_e4m3_n.argtypes = [P, P, I64]
     L.oracle_ue8m0_ceil_n.argtypes = [P, P, I64]
     L.oracle_silu_mul_n.argtypes = [P, P, P, I64]
@@ -254,6 +256,18 @@ def pack_ue8m0(scales_tg) -> np.ndarray:
     K, T_pad = -(-G // 4), -(-T // 4) * 4
     out = np.empty((K, T_pad, 4), np.uint8)
     _check(lib().oracle_pack_ue8m0(_p(s), T, G, _p(out)))
+    return out
+
+
+def pack_ue8m0_mx(scales_tg) -> np.ndarray:
+    """Power-of-two scales [T, G] -> the MXFP8 scale-factor tile layout
+    (fp8q_oracle.c), as uint8 [round_up(T, 128), 4 G]: the flat bytes in
+    storage order, shaped like the padded scale matrix they encode."""
+    s = np.ascontiguousarray(scales_tg, dtype=np.float32)
+    T, G = s.shape
+    T_pad = -(-T // 128) * 128
+    out = np.empty((T_pad, 4 * G), np.uint8)
+    _check(lib().oracle_pack_ue8m0_mx(_p(s), T, G, _p(out)))
     return out
 
 

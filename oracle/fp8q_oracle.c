@@ -443,6 +443,39 @@ int oracle_pack_ue8m0(const float *scales_tg, int64_t T, int64_t G, uint8_t *out
     return ORACLE_OK;
 }
 
+/*
+ * The same exponent bytes in the scale-factor layout of Blackwell's
+ * block-scaled (MXFP8) GEMM operands: one E8M0 byte per 32 values along the
+ * row, so a 1x128 group's byte is repeated for its four 32-value blocks; the
+ * [T_pad, 4G] byte matrix (T_pad = T rounded up to 128) is stored as tiles of
+ * 128 rows x 4 columns, tile (T_pad-row block rb, column block cb) at byte
+ * (rb * G + cb) * 512 (column blocks = G), and inside a tile the byte of row
+ * r, column c at (r % 32) * 16 + (r / 32) * 4 + c.  Column block cb is then
+ * exactly group cb.  Rows past T are 0.  Output: T_pad * 4 * G bytes.
+ */
+int oracle_pack_ue8m0_mx(const float *scales_tg, int64_t T, int64_t G, uint8_t *out)
+{
+    if (T < 0 || G <= 0)
+        return ORACLE_ERR_ARG;
+    const int64_t T_pad = (T + 127) / 128 * 128;
+    memset(out, 0, (size_t)(T_pad * 4 * G));
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t g = 0; g < G; ++g) {
+            float s = scales_tg[t * G + g];
+            int e;
+            float f = frexpf(s, &e);
+            if (f != 0.5f || e - 1 + 127 < 1 || e - 1 + 127 > 254)
+                return ORACLE_ERR_ARG;
+            for (int64_t c = 4 * g; c < 4 * g + 4; ++c) { /* the group's four 32-value blocks */
+                int64_t rb = t / 128, r = t % 128, cb = c / 4, cc = c % 4;
+                int64_t at = (rb * G + cb) * 512 + (r % 32) * 16 + (r / 32) * 4 + cc;
+                out[at] = (uint8_t)(e - 1 + 127);
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
 /* ----------------------------------------------- batch helpers (tests) -- */
 
 void oracle_f32_to_e4m3_n(const float *v, uint8_t *out, int64_t n)

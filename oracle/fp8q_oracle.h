@@ -68,6 +68,10 @@ int oracle_fused_qk_norm_rope(uint16_t *qkv, const uint16_t *q_w, const uint16_t
  * row-major powers of two -> ceil(G/4) * round_up(T,4) * 4 bytes. */
 int oracle_pack_ue8m0(const float *scales_tg, int64_t T, int64_t G, uint8_t *out);
 
+/* The MXFP8 scale-factor tile layout of the same bytes (layout in
+ * fp8q_oracle.c): round_up(T,128) * 4 * G bytes. */
+int oracle_pack_ue8m0_mx(const float *scales_tg, int64_t T, int64_t G, uint8_t *out);
+
 void oracle_f32_to_e4m3_n(const float *v, uint8_t *out, int64_t n);
 void oracle_ue8m0_ceil_n(const float *s, float *out, int64_t n);
 void oracle_silu_mul_n(const float *a, const float *b, float *out, int64_t n);

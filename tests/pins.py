@@ -392,6 +392,29 @@ def pin_ue8m0_packed_decodes():
         assert sorted(seen) == want
 
 
+def pin_ue8m0_mx_tiles():
+    """The MXFP8 tile layout against an independent construction (repeat each
+    group's exponent over its four 32-value blocks, pad rows to 128, cut
+    128 x 4 tiles, order rows inside a tile as (r % 32, r // 32)), and every
+    byte decoded back to its scale."""
+    rng = np.random.default_rng(21)
+    for T, G in [(1, 1), (5, 3), (128, 2), (130, 7), (300, 40)]:
+        s = np.ldexp(1.0, rng.integers(-30, 10, size=(T, G))).astype(np.float32)
+        got = oracle.pack_ue8m0_mx(s)
+        e = (np.frexp(s)[1] - 1 + 127).astype(np.uint8)              # exponent bytes [T, G]
+        T_pad = -(-T // 128) * 128
+        full = np.zeros((T_pad, 4 * G), np.uint8)
+        full[:T] = np.repeat(e, 4, axis=1)
+        tiles = full.reshape(T_pad // 128, 4, 32, G, 4).transpose(0, 3, 2, 1, 4)
+        assert np.array_equal(got.reshape(-1), tiles.reshape(-1)), (T, G)
+        flat = got.reshape(-1)
+        for t in range(0, T, max(1, T // 7)):
+            for g in range(G):
+                for j in range(4):
+                    at = ((t // 128) * G + g) * 512 + (t % 32) * 16 + ((t % 128) // 32) * 4 + j
+                    assert np.ldexp(1.0, int(flat[at]) - 127) == s[t, g]
+
+
 # ------------------------------------------------------- op B (rms) ----
 
 
@@ -802,6 +825,7 @@ ALL_PINS = [
     pin_golden_midpoints,
     pin_ue8m0_packed_golden,
     pin_ue8m0_packed_decodes,
+    pin_ue8m0_mx_tiles,
     pin_e4m3_roundtrip,
     pin_op_a_hand_rows,
     pin_scale_layouts,

@@ -13,6 +13,14 @@ import oracle
 import pins
 
 MUTATIONS = {
+    "mx_tile_rows_not_interleaved": (
+        "int64_t at = (rb * G + cb) * 512 + (r % 32) * 16 + (r / 32) * 4 + cc;",
+        "int64_t at = (rb * G + cb) * 512 + r * 4 + cc;",
+    ),
+    "mx_group_byte_on_one_block_only": (
+        "for (int64_t c = 4 * g; c < 4 * g + 4; ++c) {",
+        "for (int64_t c = 4 * g; c < 4 * g + 1; ++c) {",
+    ),
     "rope_sign_of_sine_term_flipped": (
         "x[ia] = oracle_f32_to_bf16(ac - bs);",
         "x[ia] = oracle_f32_to_bf16(ac + bs);",
