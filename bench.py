@@ -68,7 +68,8 @@ PER_TOKEN_OPS = {
 }
 
 
-def algorithmic_bytes(op: str, T: int, H: int, residual: bool = False, packed: bool = False) -> int:
+def algorithmic_bytes(op: str, T: int, H: int, residual: bool = False, packed: bool = False,
+                      mx: bool = False) -> int:
     """Bytes an op must move: each input read once, each output written once.
     group: x bf16 [T,H] in; e4m3 [T,H] and fp32 [T,H/128] out.
     rms:   the same plus the bf16 weight [H]; with the residual, the
@@ -76,9 +77,13 @@ def algorithmic_bytes(op: str, T: int, H: int, residual: bool = False, packed: b
     silu:  H is I; x bf16 [T,2I] in; e4m3 [T,I] and fp32 [T,I/128] out.
     packed: the scales are exponent bytes, [ceil(G/4), T rounded up to 4]
            32-bit words, instead of fp32 [T, G].
+    mx:    the scales as MXFP8 GEMM tiles, one byte per 32 values, rows
+           padded to 128: round_up(T, 128) * 4 * G bytes.
     The per-token variants move the same bytes with one fp32 scale per row."""
     G = H // GROUP
     sb = -(-G // 4) * (-(-T // 4) * 4) * 4 if packed else 4 * T * G
+    if mx:
+        sb = -(-T // 128) * 128 * 4 * G
     if op in PER_TOKEN_OPS:
         op, sb = PER_TOKEN_OPS[op], 4 * T
     if op == "per_token_group_fp8_quant":
@@ -681,17 +686,18 @@ def sweep(args):
     points.append(("rms_norm_per_block_quant", 256, 4096, False, "row", True))
     points.append(("rms_norm_per_block_quant", 256, 4096, False, "row", False))
     points.append(("silu_and_mul_per_block_quant", 1024, 12288, True, "col", False))
-    for T in (512, 4096):   # packed UE8M0 exponent bytes
-        points.append(("per_token_group_fp8_quant", T, A_H, True, "packed", False))
-        points.append(("rms_norm_per_block_quant", T, B_H, True, "packed", False))
-        points.append(("silu_and_mul_per_block_quant", T, C_I, True, "packed", False))
+    for T in (512, 4096):   # packed UE8M0 exponent bytes, and the same bytes in MXFP8 GEMM tiles
+        for lay in ("packed", "mx"):
+            points.append(("per_token_group_fp8_quant", T, A_H, True, lay, False))
+            points.append(("rms_norm_per_block_quant", T, B_H, True, lay, False))
+            points.append(("silu_and_mul_per_block_quant", T, C_I, True, lay, False))
     for T in (64, 512, 4096, 16384):   # per-token variants, one scale per row
         points.append(("dynamic_per_token_scaled_fp8_quant", T, A_H, False, "token", False))
         points.append(("rms_norm_dynamic_per_token_quant", T, B_H, False, "token", False))
         points.append(("silu_and_mul_dynamic_per_token_quant", T, C_I, False, "token", False))
     rows = []
     for op, T, H, ue8m0, lay, res in points:
-        nbytes = algorithmic_bytes(op, T, H, res, packed=lay == "packed")
+        nbytes = algorithmic_bytes(op, T, H, res, packed=lay == "packed", mx=lay == "mx")
         G = H // GROUP
 
         def make(op=op, T=T, H=H, ue8m0=ue8m0, lay=lay, res=res, G=G):
@@ -707,10 +713,12 @@ def sweep(args):
                 return lambda: fq.rms_norm_dynamic_per_token_quant(xin, w, None, ue8m0=ue8m0, q=q, scales=s)
             if lay == "packed":
                 s = torch.empty(fq.packed_scale_shape(T, G), dtype=torch.int32, device=dev)
+            elif lay == "mx":
+                s = torch.empty(fq.mx_scale_shape(T, G), dtype=torch.uint8, device=dev)
             else:
                 s = torch.empty(G, T, device=dev).t() if lay == "col" else torch.empty(T, G, device=dev)
             kw = dict(ue8m0=ue8m0, column_major_scales=lay == "col", packed_ue8m0_scales=lay == "packed",
-                      q=q, scales=s)
+                      mx_scales=lay == "mx", q=q, scales=s)
             if op == "per_token_group_fp8_quant":
                 return lambda: fq.per_token_group_fp8_quant(xin, **kw)
             if op == "silu_and_mul_per_block_quant":

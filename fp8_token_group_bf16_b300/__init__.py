@@ -40,6 +40,7 @@ FP8Q_ERR_CUDA = 4
 FP8Q_SCALES_ROW_MAJOR = 0
 FP8Q_SCALES_COL_MAJOR = 1
 FP8Q_SCALES_UE8M0_PACKED = 2
+FP8Q_SCALES_UE8M0_MX = 3
 FP8Q_RMS_MAX_H = 32768
 FP8Q_TOKEN_MAX_COLS = 65536
 GROUP = 128
@@ -182,11 +183,19 @@ def packed_scale_shape(T: int, G: int):
     return (-(-G // 4), -(-T // 4) * 4)
 
 
-def _layout(column_major_scales, packed_ue8m0_scales, ue8m0):
-    if packed_ue8m0_scales:
+def mx_scale_shape(T: int, G: int):
+    """Shape of MXFP8 scale-factor tiles as uint8: [T rounded up to 128, 4 G]
+    (the padded E8M0 matrix, one byte per 32 values, stored tile by tile)."""
+    return (-(-T // 128) * 128, 4 * G)
+
+
+def _layout(column_major_scales, packed_ue8m0_scales, ue8m0, mx_scales=False):
+    if packed_ue8m0_scales or mx_scales:
         if not ue8m0:
-            raise ValueError("packed UE8M0 scales need ue8m0=True")
-        return FP8Q_SCALES_UE8M0_PACKED
+            raise ValueError("exponent-byte scale layouts need ue8m0=True")
+        if packed_ue8m0_scales and mx_scales:
+            raise ValueError("choose one scale layout")
+        return FP8Q_SCALES_UE8M0_PACKED if packed_ue8m0_scales else FP8Q_SCALES_UE8M0_MX
     return FP8Q_SCALES_COL_MAJOR if column_major_scales else FP8Q_SCALES_ROW_MAJOR
 
 
@@ -198,6 +207,8 @@ def _outputs(x, T, cols, group_size, layout, q, scales):
     if scales is None:
         if layout == FP8Q_SCALES_UE8M0_PACKED:
             scales = torch.empty(packed_scale_shape(T, G), dtype=torch.int32, device=x.device)
+        elif layout == FP8Q_SCALES_UE8M0_MX:
+            scales = torch.empty(mx_scale_shape(T, G), dtype=torch.uint8, device=x.device)
         elif layout == FP8Q_SCALES_COL_MAJOR:
             scales = torch.empty((G, T), dtype=torch.float32, device=x.device).t()
         else:
@@ -206,6 +217,11 @@ def _outputs(x, T, cols, group_size, layout, q, scales):
 
 
 def _scale_ptr(scales, T, G, layout):
+    if layout == FP8Q_SCALES_UE8M0_MX:
+        if tuple(scales.shape) != mx_scale_shape(T, G) or scales.element_size() != 1 or \
+                not scales.is_contiguous():
+            raise ValueError(f"MX scales must be a contiguous 1-byte tensor of shape {mx_scale_shape(T, G)}")
+        return scales.data_ptr()
     if layout == FP8Q_SCALES_UE8M0_PACKED:
         if tuple(scales.shape) != packed_scale_shape(T, G) or scales.dtype != _torch().int32 or \
                 not scales.is_contiguous():
@@ -219,16 +235,18 @@ def _scale_ptr(scales, T, G, layout):
 
 def per_token_group_fp8_quant(x, group_size: int = GROUP, eps: float = 1e-10, ue8m0: bool = False,
                               column_major_scales: bool = False, q=None, scales=None, stream=None,
-                              packed_ue8m0_scales: bool = False):
+                              packed_ue8m0_scales: bool = False, mx_scales: bool = False):
     """x bf16 [T, H] (CUDA, contiguous) -> (q float8_e4m3fn [T, H], scales fp32 [T, H/g]).
 
     Column-major scales come back as a [T, G] view of a [G, T] buffer;
-    packed UE8M0 scales as int32 words [ceil(G/4), T rounded up to 4]."""
+    packed UE8M0 scales as int32 words [ceil(G/4), T rounded up to 4]; MX
+    scales as uint8 [T rounded up to 128, 4 G] in the block-scaled GEMM's
+    tile order (view them as torch.float8_e8m0fnu to hand them to such a GEMM)."""
     _need_cuda_bf16("x", x)
     if x.dim() != 2:
         raise ValueError("x must be 2-D [T, H]")
     T, H = x.shape
-    layout = _layout(column_major_scales, packed_ue8m0_scales, ue8m0)
+    layout = _layout(column_major_scales, packed_ue8m0_scales, ue8m0, mx_scales)
     q, scales = _outputs(x, T, H, group_size, layout, q, scales)
     sp = _scale_ptr(scales, T, H // max(group_size, 1), layout)
     _check(fp8q_per_token_group_quant(
@@ -239,7 +257,8 @@ def per_token_group_fp8_quant(x, group_size: int = GROUP, eps: float = 1e-10, ue
 
 def rms_norm_per_block_quant(x, weight, residual=None, eps: float = 1e-6, group_size: int = GROUP,
                              ue8m0: bool = False, column_major_scales: bool = False, q=None,
-                             scales=None, stream=None, packed_ue8m0_scales: bool = False):
+                             scales=None, stream=None, packed_ue8m0_scales: bool = False,
+                             mx_scales: bool = False):
     """RMSNorm(x [+ residual]) * weight, then group FP8 quantisation.
 
     When ``residual`` is given it is updated in place to bf16(x + residual),
@@ -253,7 +272,7 @@ def rms_norm_per_block_quant(x, weight, residual=None, eps: float = 1e-6, group_
     if x.dim() != 2 or weight.dim() != 1 or weight.shape[0] != x.shape[1]:
         raise ValueError("x must be [T, H] and weight [H]")
     T, H = x.shape
-    layout = _layout(column_major_scales, packed_ue8m0_scales, ue8m0)
+    layout = _layout(column_major_scales, packed_ue8m0_scales, ue8m0, mx_scales)
     q, scales = _outputs(x, T, H, group_size, layout, q, scales)
     sp = _scale_ptr(scales, T, H // max(group_size, 1), layout)
     _check(fp8q_rms_norm_per_block_quant(
@@ -265,13 +284,13 @@ def rms_norm_per_block_quant(x, weight, residual=None, eps: float = 1e-6, group_
 
 def silu_and_mul_per_block_quant(x, group_size: int = GROUP, eps: float = 1e-10, ue8m0: bool = False,
                                  column_major_scales: bool = False, q=None, scales=None,
-                                 stream=None, packed_ue8m0_scales: bool = False):
+                                 stream=None, packed_ue8m0_scales: bool = False, mx_scales: bool = False):
     """x bf16 [T, 2I] = [gate | up] -> quant(silu(gate) * up): (q [T, I], scales [T, I/g])."""
     _need_cuda_bf16("x", x)
     if x.dim() != 2 or x.shape[1] % 2:
         raise ValueError("x must be [T, 2I]")
     T, I = x.shape[0], x.shape[1] // 2
-    layout = _layout(column_major_scales, packed_ue8m0_scales, ue8m0)
+    layout = _layout(column_major_scales, packed_ue8m0_scales, ue8m0, mx_scales)
     q, scales = _outputs(x, T, I, group_size, layout, q, scales)
     sp = _scale_ptr(scales, T, I // max(group_size, 1), layout)
     _check(fp8q_silu_and_mul_per_block_quant(

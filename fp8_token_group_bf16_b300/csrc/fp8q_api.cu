@@ -28,9 +28,9 @@ int check_common(const void *x, const void *q, const float *scales, int64_t T, i
     if (T < 0 || H <= 0 || group_size <= 0 || H % group_size != 0)
         return FP8Q_ERR_INVALID_ARG;
     if (scale_layout != FP8Q_SCALES_ROW_MAJOR && scale_layout != FP8Q_SCALES_COL_MAJOR &&
-        scale_layout != FP8Q_SCALES_UE8M0_PACKED)
+        scale_layout != FP8Q_SCALES_UE8M0_PACKED && scale_layout != FP8Q_SCALES_UE8M0_MX)
         return FP8Q_ERR_INVALID_ARG;
-    if (scale_layout == FP8Q_SCALES_UE8M0_PACKED && !ue8m0)
+    if ((scale_layout == FP8Q_SCALES_UE8M0_PACKED || scale_layout == FP8Q_SCALES_UE8M0_MX) && !ue8m0)
         return FP8Q_ERR_INVALID_ARG;   // exponent bytes hold powers of two only
     if (group_size != kGroup)
         return FP8Q_ERR_UNSUPPORTED;
@@ -256,6 +256,8 @@ int fp8q_per_token_group_quant(const void *x, void *q, float *scales, int64_t T,
         : launch_group<U, C, false>(xp, qp, scales, n, G, T, eps, st))
     if (packed)
         e = FP8Q_GROUP(true, kPackedUe8m0);
+    else if (scale_layout == FP8Q_SCALES_UE8M0_MX)
+        e = FP8Q_GROUP(true, kMxUe8m0);
     else if (ue8m0)
         e = col ? FP8Q_GROUP(true, kColMajor) : FP8Q_GROUP(true, kRowMajor);
     else
@@ -291,6 +293,8 @@ int fp8q_silu_and_mul_per_block_quant(const void *x, void *q, float *scales, int
         : launch_silu<U, C, false>(xp, qp, scales, n, G, T, I, eps, st))
     if (packed)
         e = FP8Q_SILU(true, kPackedUe8m0);
+    else if (scale_layout == FP8Q_SCALES_UE8M0_MX)
+        e = FP8Q_SILU(true, kMxUe8m0);
     else if (ue8m0)
         e = col ? FP8Q_SILU(true, kColMajor) : FP8Q_SILU(true, kRowMajor);
     else
@@ -323,6 +327,8 @@ int fp8q_rms_norm_per_block_quant(const void *x, void *residual, const void *wei
         : launch_rms<U, C, false>(xp, rp, wp, qp, scales, t, h, G, eps, st))
     if (packed)
         e = FP8Q_RMS(true, kPackedUe8m0);
+    else if (scale_layout == FP8Q_SCALES_UE8M0_MX)
+        e = FP8Q_RMS(true, kMxUe8m0);
     else if (ue8m0)
         e = col ? FP8Q_RMS(true, kColMajor) : FP8Q_RMS(true, kRowMajor);
     else

@@ -201,10 +201,19 @@ __device__ __forceinline__ float quad_max(float m)
 //                 it, T_pad = T rounded up to a multiple of 4.  The bytes of
 //                 groups past G and of tokens past T are written as 0 by the
 //                 threads of the last group and of the last token.
+//   kMxUe8m0      the same exponent bytes in the scale-factor layout of
+//                 Blackwell's block-scaled (MXFP8) GEMM operands: one byte
+//                 per 32 values along the row, so the group's byte fills a
+//                 32-bit word (its four 32-value blocks); the [T_pad, 4G]
+//                 byte matrix (T_pad = T rounded up to 128) is stored as
+//                 128 x 4 tiles, tile (t / 128, g) at word ((t/128)*G + g)*128,
+//                 row r = t % 128 of a tile at word (r % 32) * 4 + r / 32.
+//                 The words of tokens past T are written as 0 by the thread
+//                 of the last token.
 //   kPerToken     one fp32 scale per token, s[t]; the kernels that use it
 //                 take the maximum over the whole row and store it
 //                 themselves, not through store_scale.
-constexpr int kRowMajor = 0, kColMajor = 1, kPackedUe8m0 = 2, kPerToken = 3;
+constexpr int kRowMajor = 0, kColMajor = 1, kPackedUe8m0 = 2, kMxUe8m0 = 3, kPerToken = 4;
 
 template <int LAYOUT>
 __device__ __forceinline__ void store_scale(float *scales, float s, int64_t t, int64_t g, int64_t T, int64_t G)
@@ -213,6 +222,14 @@ __device__ __forceinline__ void store_scale(float *scales, float s, int64_t t, i
         scales[t * G + g] = s;
     } else if (LAYOUT == kColMajor) {
         scales[g * T + t] = s;
+    } else if (LAYOUT == kMxUe8m0) {
+        uint32_t *w = reinterpret_cast<uint32_t *>(scales);
+        const int64_t T_pad = (T + 127) & ~int64_t(127);
+        auto word = [&](int64_t tt) { return ((tt >> 7) * G + g) * 128 + (tt & 31) * 4 + ((tt >> 5) & 3); };
+        w[word(t)] = (__float_as_uint(s) >> 23) * 0x01010101u;
+        if (t == T - 1)
+            for (int64_t tp = T; tp < T_pad; ++tp)
+                w[word(tp)] = 0;
     } else {
         uint8_t *b = reinterpret_cast<uint8_t *>(scales);
         const int64_t T_pad = (T + 3) & ~int64_t(3), G_pad = (G + 3) & ~int64_t(3);

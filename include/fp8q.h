@@ -30,8 +30,8 @@
  *    4-byte aligned.  `q` must not alias `x`; `residual` must not alias `x`.
  *  - Scale layout: FP8Q_SCALES_ROW_MAJOR stores s[t*G + g];
  *    FP8Q_SCALES_COL_MAJOR stores s[g*T + t], G = H / group_size;
- *    FP8Q_SCALES_UE8M0_PACKED stores exponent bytes (below).  A packed
- *    layout without ue8m0 is FP8Q_ERR_INVALID_ARG.
+ *    FP8Q_SCALES_UE8M0_PACKED and FP8Q_SCALES_UE8M0_MX store exponent
+ *    bytes (below).  Either without ue8m0 is FP8Q_ERR_INVALID_ARG.
  *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
  *    stream.  Calls only enqueue work and never synchronise, so they can be
  *    captured into CUDA graphs.
@@ -67,7 +67,8 @@ typedef enum {
 typedef enum {
     FP8Q_SCALES_ROW_MAJOR = 0,   /* fp32 s[t*G + g] */
     FP8Q_SCALES_COL_MAJOR = 1,   /* fp32 s[g*T + t] */
-    FP8Q_SCALES_UE8M0_PACKED = 2 /* E8M0 exponent bytes, four groups per 32-bit word (below) */
+    FP8Q_SCALES_UE8M0_PACKED = 2, /* E8M0 exponent bytes, four groups per 32-bit word (below) */
+    FP8Q_SCALES_UE8M0_MX = 3      /* E8M0 bytes in the MXFP8 GEMM scale-factor tiles (below) */
 } fp8q_scale_layout;
 
 /*
@@ -82,6 +83,20 @@ typedef enum {
  * this is the layout taken.
  */
 #define FP8Q_PACKED_SCALE_BYTES(T, G) ((((G) + 3) / 4) * (((T) + 3) / 4 * 4) * 4)
+
+/*
+ * FP8Q_SCALES_UE8M0_MX (requires ue8m0 != 0): the same exponent bytes laid
+ * out as the scale-factor operand of Blackwell's block-scaled FP8 GEMM
+ * (MXFP8: one E8M0 byte per 32 values along K, tiles of 128 rows x 4 bytes,
+ * the "32_4_4" swizzle), so the codes and these scales can be handed to such
+ * a GEMM as they are.  A group's byte is repeated for its four 32-value
+ * blocks.  The byte matrix [T_pad, 4G] (T_pad = T rounded up to 128) is
+ * stored tile by tile, tile (t/128, g) at byte ((t/128)*G + g) * 512, and
+ * inside a tile the 4 bytes of row r = t % 128 at byte (r % 32) * 16 +
+ * (r / 32) * 4.  Rows past T are written as 0.  `scales` addresses
+ * FP8Q_MX_SCALE_BYTES(T, G) bytes.
+ */
+#define FP8Q_MX_SCALE_BYTES(T, G) ((((T) + 127) / 128 * 128) * 4 * (G))
 
 /* Longest rms_norm_per_block_quant row (H) the kernels accept (a row is held
  * in the registers of one CTA). */

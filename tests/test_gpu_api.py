@@ -155,16 +155,17 @@ def test_graph_replay_matches_oracle():
 
 @pytest.mark.parametrize("T,H", [(1, 128), (5, 640), (37, 896), (130, 8320)])
 @pytest.mark.parametrize("op", ["group", "rms", "silu"])
-def test_packed_scales_no_writes_outside(T, H, op):
-    """Packed UE8M0 scales: exactly the packed bytes are written (padding
-    included), nothing around them."""
+@pytest.mark.parametrize("mx", [False, True], ids=["packed", "mx"])
+def test_packed_scales_no_writes_outside(T, H, op, mx):
+    """Exponent-byte scales (packed words or MXFP8 tiles): exactly their
+    bytes are written (padding included), nothing around them."""
     xb = inputs.bits(inputs.heavy_tailed_input(T, 2 * H if op == "silu" else H, seed=T + 7 * H))
     x = dev_bf16(xb)
     G = H // 128
-    nbytes = -(-G // 4) * (-(-T // 4) * 4) * 4
+    nbytes = (-(-T // 128) * 128 * 4 * G) if mx else -(-G // 4) * (-(-T // 4) * 4) * 4
     qraw, q = _guarded(T * H)
     sraw, s = _guarded(nbytes, torch.int32)
-    P, st = fq.FP8Q_SCALES_UE8M0_PACKED, _stream()
+    P, st = (fq.FP8Q_SCALES_UE8M0_MX if mx else fq.FP8Q_SCALES_UE8M0_PACKED), _stream()
     if op == "group":
         rc = fq.fp8q_per_token_group_quant(x.data_ptr(), q.data_ptr(), s.data_ptr(), T, H, 128, 1e-10, 1, P, st)
     elif op == "silu":

@@ -112,6 +112,34 @@ def test_packed_ue8m0_feeds_block_scaled_gemm(op, M, K, N):
     assert (out_bad[row].float() - ref[row]).abs().max() > 4 * BF16_OUT * ref.abs().max()
 
 
+@pytest.mark.parametrize("op", ["group", "rms", "silu"])
+def test_mx_tiles_feed_block_scaled_gemm_directly(op):
+    """With mx_scales=True the kernels write the scale operand of the
+    block-scaled GEMM themselves: codes and scales go in as they are."""
+    M, K, N = 300, 7168, 512
+    if op == "group":
+        x = inputs.heavy_tailed_input(M, K, seed=11).cuda()
+        q, smx = fq.per_token_group_fp8_quant(x, ue8m0=True, mx_scales=True)
+        _, s32 = fq.per_token_group_fp8_quant(x, ue8m0=True)
+    elif op == "rms":
+        x, w, _ = [t.cuda() for t in inputs.rms_input(M, K, seeds=(12, 13, 14))]
+        q, smx = fq.rms_norm_per_block_quant(x, w, ue8m0=True, mx_scales=True)
+        _, s32 = fq.rms_norm_per_block_quant(x, w, ue8m0=True)
+    else:
+        x = inputs.silu_input(M, K, seed=15).cuda()
+        q, smx = fq.silu_and_mul_per_block_quant(x, ue8m0=True, mx_scales=True)
+        _, s32 = fq.silu_and_mul_per_block_quant(x, ue8m0=True)
+    wq, ws, wb = weight_blocks(N, K, seed=16)
+    sb = swizzle_32_4_4(wb.repeat_interleave(128, dim=0).repeat_interleave(GROUP // 32, dim=1))
+    out = F.scaled_mm(q, wq.t(), smx.view(torch.float8_e8m0fnu), F.ScalingType.BlockWise1x32,
+                      sb.view(torch.float8_e8m0fnu), F.ScalingType.BlockWise1x32,
+                      swizzle_a=F.SwizzleType.SWIZZLE_32_4_4, swizzle_b=F.SwizzleType.SWIZZLE_32_4_4,
+                      output_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    ref = dequant(q, s32, 1, GROUP) @ dequant(wq, ws, 128, 128).t()
+    assert rel_err(out, ref) <= BF16_OUT
+
+
 @pytest.mark.parametrize("op", ["token", "token_silu", "token_rms"])
 def test_per_token_feeds_rowwise_gemm(op):
     M, K, N = 512, 5120, 768

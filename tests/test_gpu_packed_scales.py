@@ -106,3 +106,57 @@ def test_packed_with_ue8m0_off_is_refused():
     x = torch.zeros(4, 256, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(ValueError):
         fq.per_token_group_fp8_quant(x, packed_ue8m0_scales=True)
+
+
+# ----------------------------------- MXFP8 scale-factor tiles (kMxUe8m0) ----
+
+
+def _mx_buffer(T, G):
+    return torch.full(fq.mx_scale_shape(T, G), 0xA5, dtype=torch.uint8, device="cuda")
+
+
+@pytest.mark.parametrize("T,H", [(1, 128), (7, 896), (128, 512), (130, 7168), (4096, 7168)])
+def test_group_quant_mx_tiles(T, H):
+    xb = inputs.bits(inputs.heavy_tailed_input(T, H, 4500 + T + H))
+    x = dev_bf16(xb)
+    q, s = fq.per_token_group_fp8_quant(x, ue8m0=True, mx_scales=True, scales=_mx_buffer(T, H // 128))
+    torch.cuda.synchronize()
+    qr, sr, _ = oracle.per_token_group_quant(xb, ue8m0=True, col_major=False)
+    assert np.array_equal(host_codes(q), qr)
+    assert np.array_equal(s.cpu().numpy(), oracle.pack_ue8m0_mx(sr))   # every byte, padding rows included
+
+
+@pytest.mark.parametrize("T,H,residual", [(3, 1152, True), (200, 5120, False), (129, 4096, True)])
+def test_rms_mx_tiles(T, H, residual):
+    x, w, r = inputs.rms_input(T, H, seeds=(4600 + T, 4601 + H, 4602))
+    xb, wb = inputs.bits(x), inputs.bits(w)
+    rb = inputs.bits(r) if residual else None
+    rd = dev_bf16(rb) if residual else None
+    q, s = fq.rms_norm_per_block_quant(dev_bf16(xb), dev_bf16(wb), rd, ue8m0=True, mx_scales=True,
+                                       scales=_mx_buffer(T, H // 128))
+    torch.cuda.synchronize()
+    qr, sr, _, _, _ = oracle.rms_norm_per_block_quant(xb, wb, rb, ue8m0=True)
+    assert np.array_equal(host_codes(q), qr)
+    assert np.array_equal(s.cpu().numpy(), oracle.pack_ue8m0_mx(sr))
+
+
+@pytest.mark.parametrize("T,I", [(5, 640), (131, 1152), (64, 12288)])
+def test_silu_mx_tiles(T, I):
+    xb = inputs.bits(inputs.silu_input(T, I, seed=4700 + T + I))
+    x = dev_bf16(xb)
+    G = I // 128
+    q, s = fq.silu_and_mul_per_block_quant(x, ue8m0=True, mx_scales=True, scales=_mx_buffer(T, G))
+    _, s32 = fq.silu_and_mul_per_block_quant(x, ue8m0=True)
+    torch.cuda.synchronize()
+    # the tiles re-encode the kernel's own fp32 UE8M0 scales; those are checked against the oracle
+    assert np.array_equal(s.cpu().numpy(), oracle.pack_ue8m0_mx(s32.cpu().numpy()))
+    qr, sr, spr, vr = oracle.silu_and_mul_per_block_quant(xb, ue8m0=True, want_values=True)
+    check_fused(host_codes(q), s32.cpu().numpy(), qr, sr, spr, vr, True, f"silu mx T={T} I={I}")
+
+
+def test_mx_and_packed_need_ue8m0():
+    x = torch.zeros(4, 256, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ValueError):
+        fq.per_token_group_fp8_quant(x, mx_scales=True)
+    with pytest.raises(ValueError):
+        fq.per_token_group_fp8_quant(x, ue8m0=True, mx_scales=True, packed_ue8m0_scales=True)

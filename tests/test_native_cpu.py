@@ -77,7 +77,7 @@ def test_rejects_bad_shapes(lib):
     assert fq.fp8q_per_token_group_quant(A, Q, S, -1, 512, 128, 1e-10, 0, 0, None) == E
     assert fq.fp8q_per_token_group_quant(A, Q, S, 4, 0, 128, 1e-10, 0, 0, None) == E
     assert fq.fp8q_per_token_group_quant(A, Q, S, 4, 500, 128, 1e-10, 0, 0, None) == E
-    assert fq.fp8q_per_token_group_quant(A, Q, S, 4, 512, 128, 1e-10, 0, 3, None) == E
+    assert fq.fp8q_per_token_group_quant(A, Q, S, 4, 512, 128, 1e-10, 0, 5, None) == E
     assert fq.fp8q_per_token_group_quant(None, Q, S, 4, 512, 128, 1e-10, 0, 0, None) == E
     assert fq.fp8q_silu_and_mul_per_block_quant(A, Q, S, 4, 100, 128, 1e-10, 0, 0, None) == E
     assert fq.fp8q_rms_norm_per_block_quant(A, None, None, Q, S, 4, 512, 128, 1e-6, 0, 0, None) == E
@@ -93,6 +93,12 @@ def test_packed_scales_need_ue8m0(lib):
     assert fq.fp8q_rms_norm_per_block_quant(A, None, A, Q, S, 4, 512, 128, 1e-6, 0, P, None) == E
     # with ue8m0 it passes the checks: an empty input is then a no-op
     assert fq.fp8q_per_token_group_quant(None, None, None, 0, 512, 128, 1e-10, 1, P, None) == 0
+    X = fq.FP8Q_SCALES_UE8M0_MX   # the MXFP8 tile layout likewise
+    assert fq.fp8q_per_token_group_quant(A, Q, S, 4, 512, 128, 1e-10, 0, X, None) == E
+    assert fq.fp8q_silu_and_mul_per_block_quant(A, Q, S, 4, 512, 128, 1e-10, 0, X, None) == E
+    assert fq.fp8q_rms_norm_per_block_quant(A, None, A, Q, S, 4, 512, 128, 1e-6, 0, X, None) == E
+    assert fq.fp8q_per_token_group_quant(None, None, None, 0, 512, 128, 1e-10, 1, X, None) == 0
+    assert fq.fp8q_per_token_group_quant(A, Q, S, 4, 512, 128, 1e-10, 1, 4, None) == E
 
 
 def test_packed_scale_shape():
@@ -105,6 +111,10 @@ def test_packed_scale_shape():
     for T, G in [(5, 6), (4096, 56), (1, 1), (7, 192)]:
         k, tp = fq.packed_scale_shape(T, G)
         assert k * tp * 4 == (((G) + 3) // 4) * (((T) + 3) // 4 * 4) * 4
+    assert "#define FP8Q_MX_SCALE_BYTES(T, G) ((((T) + 127) / 128 * 128) * 4 * (G))" in text
+    for T, G in [(5, 6), (4096, 56), (1, 1), (129, 200)]:
+        r, c = fq.mx_scale_shape(T, G)
+        assert r * c == (((T) + 127) // 128 * 128) * 4 * (G) and r % 128 == 0 and c == 4 * G
 
 
 def test_per_token_checks(lib):
