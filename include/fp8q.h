@@ -1,5 +1,6 @@
 /*
- * libfp8q — fused FP8 per-group quantisation epilogues for NVIDIA B300 (sm_103a).
+ * libfp8q — fused FP8 quantisation epilogues (and the fused QK-norm + rotary
+ * embedding) for NVIDIA B300 (sm_103a).
  *
  * The three operations are the FP8 activation-quantisation custom ops of FP8
  * LLM inference named in "[RFC]: Using Helion for Selected vLLM CustomOps"
@@ -19,6 +20,11 @@
  *          subnormals kept, sign of zero kept.
  * The pages print no formula; this is the plain reading, and the library
  * reproduces it bit for bit for per_token_group_quant.
+ *
+ * Beside the three per-group ops the library holds their per-token variants
+ * (one scale per token row) and fused_qk_norm_rope, from the list of kernels
+ * in "Helion-Kernel in vLLM: PyTorch FP8 ohne CUDA" (section "Welche Kernel
+ * wurden in vLLM integriert"); each is specified at its declaration below.
  *
  * Conventions shared by every entry point:
  *  - Pointers are DEVICE pointers (global memory of the current device).  The
