@@ -113,8 +113,8 @@ template <bool U, int C, bool V>
 cudaError_t launch_silu(const uint16_t *x, uint8_t *q, float *s, int64_t n, int64_t G, int64_t T,
                         int64_t I, float eps, cudaStream_t st)
 {
-    return launch(silu_quant_kernel<U, C, V>, dim3{unsigned((n + kGroupsPerCta - 1) / kGroupsPerCta)},
-                  dim3{unsigned(kCtaThreads)}, st, x, q, s, n, G, T, I, eps);
+    return launch(silu_quant_kernel<U, C, V>, dim3{unsigned((n + kSiluGroupsPerCta - 1) / kSiluGroupsPerCta)},
+                  dim3{unsigned(kSiluCtaThreads)}, st, x, q, s, n, G, T, I, eps);
 }
 
 // rms_norm_per_block_quant, one CTA per row with the row in registers: one
@@ -414,7 +414,8 @@ int fp8q_fused_qk_norm_rope(void *qkv, const void *q_weight, const void *k_weigh
     auto kw = static_cast<const uint16_t *>(k_weight);
     auto cs = static_cast<const uint16_t *>(cos_sin);
     constexpr int kLph = FP8Q_ROPE_LANES;   // lanes per head
-    const dim3 grid{unsigned((n + 256 / kLph - 1) / (256 / kLph))}, block{256};
+    constexpr int kUpc = kRopeCtaThreads / kLph;   // units per CTA
+    const dim3 grid{unsigned((n + kUpc - 1) / kUpc)}, block{unsigned(kRopeCtaThreads)};
     auto st = static_cast<cudaStream_t>(stream);
     const int nhi = int(nh), hq = int(num_q_heads);
     cudaError_t e;
