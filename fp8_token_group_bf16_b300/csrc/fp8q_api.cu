@@ -104,9 +104,9 @@ template <bool U, int C, bool V>
 cudaError_t launch_group(const uint16_t *x, uint8_t *q, float *s, int64_t n, int64_t G, int64_t T,
                          float eps, cudaStream_t st)
 {
-    const int64_t per = int64_t(kGroupsPerCta) * kGroupQuantGpt;
+    const int64_t per = int64_t(kGroupQuantGroupsPerCta) * kGroupQuantGpt;
     return launch(group_quant_kernel<U, C, V>, dim3{unsigned((n + per - 1) / per)},
-                  dim3{unsigned(kCtaThreads)}, st, x, q, s, n, G, T, eps);
+                  dim3{unsigned(kGroupCtaThreads)}, st, x, q, s, n, G, T, eps);
 }
 
 template <bool U, int C, bool V>

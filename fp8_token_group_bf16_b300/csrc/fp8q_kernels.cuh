@@ -12,7 +12,14 @@ namespace fp8q {
 
 constexpr int kCtaThreads = 256;                               // ops A and C
 constexpr int kGroupsPerCta = kCtaThreads / kLanesPerGroup;    // 64
-constexpr int kGroupQuantGpt = 2;                              // groups per quad, op A
+// Op A in CTAs of two warps, one group per quad (16 groups per CTA).
+// Measured at T = 4096, H = 7168 (UE8M0 column-major / fp32 row-major
+// scales): 15.35 / 15.44 us, against 15.8 / 15.55 us with 256-thread CTAs
+// and two groups per quad; 3.29 against 3.50 us at T = 512.  Four groups per
+// quad: 16.3 us.
+constexpr int kGroupQuantGpt = 1;                              // groups per quad, op A
+constexpr int kGroupCtaThreads = 64;
+constexpr int kGroupQuantGroupsPerCta = kGroupCtaThreads / kLanesPerGroup;   // 16
 // Op C in CTAs of two warps (16 groups): 64 registers a thread allow 16 such
 // CTAs per SM.  Measured at T = 4096, I = 25600: 82.8 us, against 83.4 us
 // with 128-thread and 85.9 us with 256-thread CTAs (the same 32 warps per SM
@@ -35,13 +42,13 @@ __device__ __forceinline__ void split_group(int64_t gi, int64_t G, int64_t &t, i
 // per_token_group_fp8_quant
 //
 // A contiguous [T, H] tensor is a flat sequence of T*G groups, so the kernel
-// walks groups, not rows.  CTA b owns groups [b*64*GPT, (b+1)*64*GPT); quad q
-// of the CTA takes groups b*64*GPT + j*64 + q for j < GPT, so the 8 quads of
+// walks groups, not rows.  CTA b owns groups [b*16*GPT, (b+1)*16*GPT); quad q
+// of the CTA takes groups b*16*GPT + j*16 + q for j < GPT, so the 8 quads of
 // a warp read 8 adjacent groups (2 KiB) per pair of load instructions.
 // Out-of-range quads load a clamped, valid group and store nothing.
 // --------------------------------------------------------------------------
 template <bool UE8M0, int LAYOUT, bool V8>
-__global__ void __launch_bounds__(kCtaThreads) group_quant_kernel(const uint16_t *__restrict__ x,
+__global__ void __launch_bounds__(kGroupCtaThreads) group_quant_kernel(const uint16_t *__restrict__ x,
                                                                   uint8_t *__restrict__ q,
                                                                   float *__restrict__ scales,
                                                                   int64_t n_groups, int64_t G,
@@ -49,20 +56,20 @@ __global__ void __launch_bounds__(kCtaThreads) group_quant_kernel(const uint16_t
 {
     constexpr int GPT = kGroupQuantGpt;
     const int sub = threadIdx.x & (kLanesPerGroup - 1);
-    const int64_t first = int64_t(blockIdx.x) * kGroupsPerCta * GPT + (threadIdx.x / kLanesPerGroup);
+    const int64_t first = int64_t(blockIdx.x) * kGroupQuantGroupsPerCta * GPT + (threadIdx.x / kLanesPerGroup);
 
     wait_for_producer();
     allow_consumer_launch();
     uint32_t raw[GPT][16];
 #pragma unroll
     for (int j = 0; j < GPT; ++j) {
-        const int64_t gi = first + int64_t(j) * kGroupsPerCta;
+        const int64_t gi = first + int64_t(j) * kGroupQuantGroupsPerCta;
         const int64_t gl = gi < n_groups ? gi : n_groups - 1;
         ld64_stream<V8>(x + gl * kGroup + sub * kValsPerLane, raw[j]);
     }
 #pragma unroll
     for (int j = 0; j < GPT; ++j) {
-        const int64_t gi = first + int64_t(j) * kGroupsPerCta;
+        const int64_t gi = first + int64_t(j) * kGroupQuantGroupsPerCta;
         uint64_t v[16];
         float m = 0.0f;
 #pragma unroll
