@@ -12,14 +12,15 @@ namespace fp8q {
 
 constexpr int kCtaThreads = 256;                               // ops A and C
 constexpr int kGroupsPerCta = kCtaThreads / kLanesPerGroup;    // 64
-// Op A in CTAs of two warps, one group per quad (16 groups per CTA).
-// Measured at T = 4096, H = 7168 (UE8M0 column-major / fp32 row-major
-// scales): 15.35 / 15.44 us, against 15.8 / 15.55 us with 256-thread CTAs
-// and two groups per quad; 3.29 against 3.50 us at T = 512.  Four groups per
-// quad: 16.3 us.
+// Op A in CTAs of four warps, one group per quad (32 groups per CTA).
+// Measured (UE8M0 column-major / fp32 row-major scales, H = 7168): T = 4096
+// 15.45 / 15.01 us, T = 16384 54.3 / 53.4 us, T = 512 3.28 / 3.89 us;
+// 256-thread CTAs with two groups per quad: 15.6 / 15.6, 54.6 / 54.1,
+// 3.48 / 4.18 us.  64-thread CTAs match at T = 4096 but reach 59.3 us at
+// T = 16384 (57,344 CTAs of 4 KiB: the CTA launch rate, not HBM, limits).
 constexpr int kGroupQuantGpt = 1;                              // groups per quad, op A
-constexpr int kGroupCtaThreads = 64;
-constexpr int kGroupQuantGroupsPerCta = kGroupCtaThreads / kLanesPerGroup;   // 16
+constexpr int kGroupCtaThreads = 128;
+constexpr int kGroupQuantGroupsPerCta = kGroupCtaThreads / kLanesPerGroup;   // 32
 // Op C in CTAs of two warps (16 groups): 64 registers a thread allow 16 such
 // CTAs per SM.  Measured at T = 4096, I = 25600: 82.8 us, against 83.4 us
 // with 128-thread and 85.9 us with 256-thread CTAs (the same 32 warps per SM
@@ -42,8 +43,8 @@ __device__ __forceinline__ void split_group(int64_t gi, int64_t G, int64_t &t, i
 // per_token_group_fp8_quant
 //
 // A contiguous [T, H] tensor is a flat sequence of T*G groups, so the kernel
-// walks groups, not rows.  CTA b owns groups [b*16*GPT, (b+1)*16*GPT); quad q
-// of the CTA takes groups b*16*GPT + j*16 + q for j < GPT, so the 8 quads of
+// walks groups, not rows.  CTA b owns groups [b*32*GPT, (b+1)*32*GPT); quad q
+// of the CTA takes groups b*32*GPT + j*32 + q for j < GPT, so the 8 quads of
 // a warp read 8 adjacent groups (2 KiB) per pair of load instructions.
 // Out-of-range quads load a clamped, valid group and store nothing.
 // --------------------------------------------------------------------------
