@@ -31,6 +31,15 @@ def test_algorithmic_bytes_per_element():
     assert bench.algorithmic_bytes("per_token_group_fp8_quant", 5, 768, packed=True) == 5 * 768 * 3 + 2 * 8 * 4
     assert bench.algorithmic_bytes("silu_and_mul_per_block_quant", 4096, 25600, packed=True) == \
         4096 * 25600 * 5 + 4096 * 200
+    # MXFP8 tiles: four bytes per group (one per 32 values), rows padded to 128
+    assert bench.algorithmic_bytes("per_token_group_fp8_quant", 130, 7168, mx=True) == 130 * 7168 * 3 + 256 * 4 * 56
+    # per-token variants: one fp32 scale per row
+    assert bench.algorithmic_bytes("dynamic_per_token_scaled_fp8_quant", 7, 896) == 7 * 896 * 3 + 4 * 7
+    assert bench.algorithmic_bytes("rms_norm_dynamic_per_token_quant", 7, 896, residual=True) == \
+        7 * 896 * 3 + 4 * 7 + 2 * 896 + 4 * 7 * 896
+    assert bench.algorithmic_bytes("silu_and_mul_dynamic_per_token_quant", 7, 896) == 7 * 896 * 5 + 4 * 7
+    # fused_qk_norm_rope: heads read and written, position and table row per token, two weights
+    assert bench.qk_rope_bytes(10) == 10 * (72 * 128 * 4 + 8 + 256) + 512
     assert bench.step_bytes(1) == 21728 + 15520 + 10240 + 128800
 
 
