@@ -54,6 +54,7 @@ EXPORTS = (
     "fp8q_silu_and_mul_dynamic_per_token_quant",
     "fp8q_fused_qk_norm_rope",
     "fp8q_f32_to_e4m3",
+    "fp8q_silu_mul",
     "fp8q_status_string",
     "fp8q_version",
 )
@@ -86,7 +87,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.fp8q_silu_and_mul_dynamic_per_token_quant.argtypes = [P, P, P, I64, I64, F, I32, P]
     L.fp8q_fused_qk_norm_rope.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, F, I32, P]
     L.fp8q_f32_to_e4m3.argtypes = [P, P, I64, P]
-    for n in EXPORTS[:8]:
+    L.fp8q_silu_mul.argtypes = [P, P, P, I64, P]
+    for n in EXPORTS[:9]:
         getattr(L, n).restype = ctypes.c_int
     L.fp8q_status_string.argtypes = [ctypes.c_int]
     L.fp8q_status_string.restype = ctypes.c_char_p
@@ -137,6 +139,10 @@ def fp8q_fused_qk_norm_rope(qkv, q_weight, k_weight, cos_sin, positions, T, num_
 
 def fp8q_f32_to_e4m3(v, out, n, stream):
     return load().fp8q_f32_to_e4m3(v, out, n, stream)
+
+
+def fp8q_silu_mul(a, b, out, n, stream):
+    return load().fp8q_silu_mul(a, b, out, n, stream)
 
 
 def fp8q_status_string(status: int) -> str:
@@ -387,6 +393,20 @@ def fused_qk_norm_rope(qkv, q_weight, k_weight, cos_sin, positions, num_q_heads:
                                    positions.data_ptr(), T, num_q_heads, num_kv_heads, head_dim, cos_sin.shape[0],
                                    eps, int(is_neox), _stream_ptr(qkv, stream)), "fused_qk_norm_rope")
     return qkv
+
+
+def silu_mul(a, b, out=None, stream=None):
+    """fp32 CUDA tensors a, b (same shape) -> silu(a) * b as op C computes it."""
+    torch = _torch()
+    for name, t in (("a", a), ("b", b)):
+        if t.device.type != "cuda" or t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous fp32 CUDA tensor")
+    if a.shape != b.shape:
+        raise ValueError("a and b must have the same shape")
+    if out is None:
+        out = torch.empty_like(a)
+    _check(fp8q_silu_mul(a.data_ptr(), b.data_ptr(), out.data_ptr(), a.numel(), _stream_ptr(a, stream)), "silu_mul")
+    return out
 
 
 def f32_to_e4m3(v, out=None, stream=None):

@@ -447,6 +447,23 @@ int fp8q_f32_to_e4m3(const float *v, void *out, int64_t n, void *stream)
     return launch_status(cudaSuccess);
 }
 
+int fp8q_silu_mul(const float *a, const float *b, float *out, int64_t n, void *stream)
+{
+    if (n < 0)
+        return FP8Q_ERR_INVALID_ARG;
+    if (n == 0)
+        return FP8Q_OK;
+    if (!a || !b || !out)
+        return FP8Q_ERR_INVALID_ARG;
+    if (!aligned(a, 8) || !aligned(b, 8) || !aligned(out, 8))
+        return FP8Q_ERR_MISALIGNED;
+    const int64_t blocks = ((n + 1) / 2 + 255) / 256;
+    if (blocks > 0x7FFFFFFF)
+        return FP8Q_ERR_UNSUPPORTED;
+    silu_mul_kernel<<<dim3{unsigned(blocks)}, 256, 0, static_cast<cudaStream_t>(stream)>>>(a, b, out, n);
+    return launch_status(cudaSuccess);
+}
+
 const char *fp8q_status_string(int status)
 {
     switch (status) {

@@ -104,15 +104,16 @@ __global__ void __launch_bounds__(kGroupCtaThreads) group_quant_kernel(const uin
 // x[t, g*128 ...] and the up values x[t, I + g*128 ...] (64 bytes of each per
 // lane, both loads issued first).
 //
-// v = RN32(RN32(a / d) * b) with d = RN32(1 + expf(-a)).  The quotient is
+// v = RN32(RN32(a / d) * b) with d = RN32(1 + e^-a).  The quotient is
 // formed from r = rcp.approx(d) with one residual correction,
 // q = q0 + RN32(a - q0 d) r, q0 = RN32(a r) (Newton-Raphson on the quotient;
 // the residual is exact by FMA), which is the correctly rounded a / d except
 // in rare cases where it is one ulp off, and is cheaper than IEEE division.
-// expf's argument is capped at 88 (e^88 < FLT_MAX) so that d stays finite:
-// for a below -88 the exact result is a negative number below 1e-36 (or -0),
-// whose code is a zero of the same sign either way.  Pairs of values go
-// through packed fp32x2 instructions.
+// The exponential's argument is capped at 88 (e^88 < FLT_MAX) so that d
+// stays finite: for a below -88 the exact result is a negative number below
+// 1e-36 (or -0), whose code is a zero of the same sign either way.  Below
+// -104 it is floored (e^-104 rounds to 0 in fp32 either way).  Pairs of
+// values go through packed fp32x2 instructions.
 // --------------------------------------------------------------------------
 __device__ __forceinline__ float rcp_approx(float d)
 {
@@ -121,12 +122,45 @@ __device__ __forceinline__ float rcp_approx(float d)
     return r;
 }
 
-__device__ __forceinline__ uint64_t silu_mul2(uint32_t aw, uint32_t bw)
+__device__ __forceinline__ float ex2_approx(float t)
 {
-    const uint64_t a = f2_from_bf16x2(aw), b = f2_from_bf16x2(bw);
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
+    return r;
+}
+
+// e^x for a pair of x in [-104, 88], as 2^(x log2 e).  The product x log2 e is
+// carried as th + tl: th = RN32(x L) with L = RN32(log2 e), tl its exact
+// rounding error (one FMA, the TwoProduct of Ogita, Rump and Oishi) plus
+// x (log2 e - L); then e^x = 2^th 2^tl ~ 2^th (1 + tl ln 2), with 2^th from
+// the PTX ex2.approx instruction (|tl| < 2^-17 here, so the dropped
+// second-order term is below 2^-35 relative).  The error is that of
+// ex2.approx plus two roundings; the tests measure it against the libm
+// expf of the oracle over every bf16 argument.  It replaces a call of expf,
+// whose extra instructions cost 5 % of the whole op in this issue-bound
+// kernel.
+__device__ __forceinline__ uint64_t exp_f2(uint64_t x)
+{
+    constexpr float kLog2e = 1.44269502f;       // RN32(log2 e)
+    constexpr float kLog2eLo = 1.925963e-08f;   // log2 e - kLog2e
+    constexpr float kLn2 = 0.693147182f;        // RN32(ln 2)
+    const uint64_t nth = f2_mul(x, f2_pack(-kLog2e, -kLog2e));           // -th
+    uint64_t tl = f2_fma(x, f2_pack(kLog2e, kLog2e), nth);               // x L - th, exact
+    tl = f2_fma(x, f2_pack(kLog2eLo, kLog2eLo), tl);
+    float n0, n1;
+    f2_unpack(nth, n0, n1);
+    const uint64_t p = f2_pack(ex2_approx(-n0), ex2_approx(-n1));
+    return f2_fma(p, f2_mul(tl, f2_pack(kLn2, kLn2)), p);
+}
+
+// silu(a) * b for a pair of fp32 values a, b.
+__device__ __forceinline__ uint64_t silu_mul_f2(uint64_t a, uint64_t b)
+{
     float a0, a1;
     f2_unpack(a, a0, a1);
-    const uint64_t e = f2_pack(expf(fminf(-a0, 88.0f)), expf(fminf(-a1, 88.0f)));
+    // -a clamped to [-104, 88]: e^-104 is below the smallest fp32 subnormal,
+    // and the bound keeps x log2 e finite for any finite a
+    const uint64_t e = exp_f2(f2_pack(fminf(fmaxf(-a0, -104.0f), 88.0f), fminf(fmaxf(-a1, -104.0f), 88.0f)));
     const uint64_t d = f2_add(f2_pack(1.0f, 1.0f), e);
     const uint64_t nd = f2_sub(f2_pack(-1.0f, -1.0f), e);   // exactly -d
     float d0, d1;
@@ -136,6 +170,11 @@ __device__ __forceinline__ uint64_t silu_mul2(uint32_t aw, uint32_t bw)
     const uint64_t res = f2_fma(q0, nd, a);
     const uint64_t q = f2_fma(res, r, q0);
     return f2_mul(q, b);
+}
+
+__device__ __forceinline__ uint64_t silu_mul2(uint32_t aw, uint32_t bw)
+{
+    return silu_mul_f2(f2_from_bf16x2(aw), f2_from_bf16x2(bw));
 }
 
 template <bool UE8M0, int LAYOUT, bool V8>
@@ -195,6 +234,27 @@ __global__ void __launch_bounds__(256) f32_to_e4m3_kernel(const float *__restric
             const uint32_t c = pack4_e4m3(v[i], 0.f, 0.f, 0.f);
             out[i] = uint8_t(c & 0xFFu);
         }
+    }
+}
+
+// --------------------------------------------------------------------------
+// Elementwise silu(a) * b in fp32, the value op C quantises (for checking
+// the arithmetic on its own).  Thread i takes elements 2i and 2i + 1 (the
+// second only if it exists); a, b, out 8-byte aligned.
+// --------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) silu_mul_kernel(const float *__restrict__ a, const float *__restrict__ b,
+                                                       float *__restrict__ out, int64_t n)
+{
+    const int64_t i = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) * 2;
+    if (i + 1 < n) {
+        const float2 av = *reinterpret_cast<const float2 *>(a + i), bv = *reinterpret_cast<const float2 *>(b + i);
+        float o0, o1;
+        f2_unpack(silu_mul_f2(f2_pack(av.x, av.y), f2_pack(bv.x, bv.y)), o0, o1);
+        *reinterpret_cast<float2 *>(out + i) = make_float2(o0, o1);
+    } else if (i < n) {
+        float o0, o1;
+        f2_unpack(silu_mul_f2(f2_pack(a[i], 0.0f), f2_pack(b[i], 0.0f)), o0, o1);
+        out[i] = o0;
     }
 }
 

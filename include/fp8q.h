@@ -154,8 +154,8 @@ FP8Q_API int fp8q_rms_norm_per_block_quant(const void *x, void *residual, const 
  *   q       e4m3 [T, I], written.
  *   scales  fp32 [T*I/group_size] in `scale_layout`, written.
  *   eps     amax floor, as for per_token_group_quant.
- * v = RN32(RN32(a / RN32(1 + expf(-a))) * b) with CUDA's expf (within 2 ulp
- * of exp), then the group quantisation of v.
+ * v = RN32(RN32(a / RN32(1 + e^-a)) * b) (e^-a and the quotient as
+ * fp8q_silu_mul states), then the group quantisation of v.
  */
 FP8Q_API int fp8q_silu_and_mul_per_block_quant(const void *x, void *q, float *scales, int64_t T, int64_t I,
                                       int32_t group_size, float eps, int32_t ue8m0,
@@ -233,6 +233,17 @@ FP8Q_API int fp8q_fused_qk_norm_rope(void *qkv, const void *q_weight, const void
  * aligned.  Exposed so the rounding can be checked on its own.
  */
 FP8Q_API int fp8q_f32_to_e4m3(const float *v, void *out, int64_t n, void *stream);
+
+/*
+ * Elementwise out[i] = silu(a[i]) * b[i] in fp32, computed exactly as
+ * silu_and_mul_per_block_quant computes the value it quantises:
+ * RN32(RN32(a / RN32(1 + e^-a)) * b), the exponential from 2^(-a log2 e)
+ * (PTX ex2.approx with the product's rounding error corrected), the quotient
+ * from an approximate reciprocal with one exact-residual step.  Exposed so
+ * the arithmetic can be checked on its own.  a, b, out: fp32 [n], 8-byte
+ * aligned.
+ */
+FP8Q_API int fp8q_silu_mul(const float *a, const float *b, float *out, int64_t n, void *stream);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 FP8Q_API const char *fp8q_status_string(int status);

@@ -186,6 +186,9 @@ def test_misaligned(lib):
     assert fq.fp8q_rms_norm_per_block_quant(A, A + 8, A, Q, S, 4, 512, 128, 1e-6, 0, 0, None) == M
     assert fq.fp8q_rms_norm_per_block_quant(A, None, A + 2, Q, S, 4, 512, 128, 1e-6, 0, 0, None) == M
     assert fq.fp8q_f32_to_e4m3(A + 4, Q, 16, None) == M
+    assert fq.fp8q_silu_mul(A + 4, A, A, 16, None) == M
+    assert fq.fp8q_silu_mul(A, A, A, -1, None) == fq.FP8Q_ERR_INVALID_ARG
+    assert fq.fp8q_silu_mul(None, None, None, 0, None) == 0
 
 
 def test_empty_input_is_a_no_op(lib):
