@@ -100,21 +100,26 @@ cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t
     return launch_ex(kernel, grid, block, 1u, 0, st, args...);
 }
 
-template <bool U, int C, bool V>
-cudaError_t launch_group(const uint16_t *x, uint8_t *q, float *s, int64_t n, int64_t G, int64_t T,
-                         float eps, cudaStream_t st)
+// Grid of a group kernel with Q groups per CTA (see group_of).
+template <bool TOKEN_MAJOR, int Q>
+dim3 group_grid(int64_t T, int64_t G)
 {
-    const int64_t per = int64_t(kGroupQuantGroupsPerCta) * kGroupQuantGpt;
-    return launch(group_quant_kernel<U, C, V>, dim3{unsigned((n + per - 1) / per)},
-                  dim3{unsigned(kGroupCtaThreads)}, st, x, q, s, n, G, T, eps);
+    return TOKEN_MAJOR ? dim3{unsigned((T + Q - 1) / Q * G)} : dim3{unsigned((T * G + Q - 1) / Q)};
 }
 
 template <bool U, int C, bool V>
-cudaError_t launch_silu(const uint16_t *x, uint8_t *q, float *s, int64_t n, int64_t G, int64_t T,
-                        int64_t I, float eps, cudaStream_t st)
+cudaError_t launch_group(const uint16_t *x, uint8_t *q, float *s, int64_t G, int64_t T, float eps, cudaStream_t st)
 {
-    return launch(silu_quant_kernel<U, C, V>, dim3{unsigned((n + kSiluGroupsPerCta - 1) / kSiluGroupsPerCta)},
-                  dim3{unsigned(kSiluCtaThreads)}, st, x, q, s, n, G, T, I, eps);
+    return launch(group_quant_kernel<U, C, V>, group_grid<kGroupTokenMajor<U, C>, kGroupQuantGroupsPerCta>(T, G),
+                  dim3{unsigned(kGroupCtaThreads)}, st, x, q, s, G, T, eps);
+}
+
+template <bool U, int C, bool V>
+cudaError_t launch_silu(const uint16_t *x, uint8_t *q, float *s, int64_t G, int64_t T, int64_t I, float eps,
+                        cudaStream_t st)
+{
+    return launch(silu_quant_kernel<U, C, V>, group_grid<false, kSiluGroupsPerCta>(T, G),
+                  dim3{unsigned(kSiluCtaThreads)}, st, x, q, s, G, T, I, eps);
 }
 
 // rms_norm_per_block_quant, one CTA per row with the row in registers: one
@@ -243,7 +248,6 @@ int fp8q_per_token_group_quant(const void *x, void *q, float *scales, int64_t T,
     const int64_t G = H / kGroup;
     if ((rc = check_groups(T, G)) != FP8Q_OK)
         return rc;
-    const int64_t n = T * G;
     auto st = static_cast<cudaStream_t>(stream);
     auto xp = static_cast<const uint16_t *>(x);
     auto qp = static_cast<uint8_t *>(q);
@@ -252,8 +256,8 @@ int fp8q_per_token_group_quant(const void *x, void *q, float *scales, int64_t T,
     const bool v8 = aligned(x, 32) && aligned(q, 32);
     cudaError_t e;
 #define FP8Q_GROUP(U, C)                                                                         \
-    (v8 ? launch_group<U, C, true>(xp, qp, scales, n, G, T, eps, st)                            \
-        : launch_group<U, C, false>(xp, qp, scales, n, G, T, eps, st))
+    (v8 ? launch_group<U, C, true>(xp, qp, scales, G, T, eps, st)                               \
+        : launch_group<U, C, false>(xp, qp, scales, G, T, eps, st))
     if (packed)
         e = FP8Q_GROUP(true, kPackedUe8m0);
     else if (scale_layout == FP8Q_SCALES_UE8M0_MX)
@@ -280,7 +284,6 @@ int fp8q_silu_and_mul_per_block_quant(const void *x, void *q, float *scales, int
     const int64_t G = I / kGroup;
     if ((rc = check_groups(T, G)) != FP8Q_OK)
         return rc;
-    const int64_t n = T * G;
     auto st = static_cast<cudaStream_t>(stream);
     auto xp = static_cast<const uint16_t *>(x);
     auto qp = static_cast<uint8_t *>(q);
@@ -289,8 +292,8 @@ int fp8q_silu_and_mul_per_block_quant(const void *x, void *q, float *scales, int
     const bool v8 = aligned(x, 32) && aligned(q, 32);
     cudaError_t e;
 #define FP8Q_SILU(U, C)                                                                          \
-    (v8 ? launch_silu<U, C, true>(xp, qp, scales, n, G, T, I, eps, st)                          \
-        : launch_silu<U, C, false>(xp, qp, scales, n, G, T, I, eps, st))
+    (v8 ? launch_silu<U, C, true>(xp, qp, scales, G, T, I, eps, st)                             \
+        : launch_silu<U, C, false>(xp, qp, scales, G, T, I, eps, st))
     if (packed)
         e = FP8Q_SILU(true, kPackedUe8m0);
     else if (scale_layout == FP8Q_SCALES_UE8M0_MX)

@@ -16,10 +16,13 @@ constexpr int kGroupsPerCta = kCtaThreads / kLanesPerGroup;    // 64
 // Measured (UE8M0 column-major / fp32 row-major scales, H = 7168): T = 4096
 // 15.45 / 15.01 us, T = 16384 54.3 / 53.4 us, T = 512 3.28 / 3.89 us;
 // 256-thread CTAs with two groups per quad: 15.6 / 15.6, 54.6 / 54.1,
-// 3.48 / 4.18 us.  64-thread CTAs match at T = 4096 but reach 59.3 us at
-// T = 16384 (57,344 CTAs of 4 KiB: the CTA launch rate, not HBM, limits).
-constexpr int kGroupQuantGpt = 1;                              // groups per quad, op A
+// 3.48 / 4.18 us; four groups per quad: 16.3 us at T = 4096.  64-thread CTAs
+// match at T = 4096 but reach 59.3 us at T = 16384 (57,344 CTAs of 4 KiB: the
+// CTA launch rate, not HBM, limits).
 constexpr int kGroupCtaThreads = 128;
+// Op A walks token-major tiles only for UE8M0 column-major scales (group_of).
+template <bool UE8M0, int LAYOUT>
+constexpr bool kGroupTokenMajor = UE8M0 && LAYOUT == kColMajor;
 constexpr int kGroupQuantGroupsPerCta = kGroupCtaThreads / kLanesPerGroup;   // 32
 // Op C in CTAs of two warps (16 groups): 64 registers a thread allow 16 such
 // CTAs per SM.  Measured at T = 4096, I = 25600: 82.8 us, against 83.4 us
@@ -39,61 +42,80 @@ __device__ __forceinline__ void split_group(int64_t gi, int64_t G, int64_t &t, i
     g = gi - int64_t(tt) * G;
 }
 
+// The group that quad `quad` of CTA `b` owns, Q quads per CTA; false (and a
+// valid group to load) when the quad is past the end.  Flat order
+// (TOKEN_MAJOR false): consecutive quads on consecutive groups of a row.
+// Token-major tiles (TOKEN_MAJOR true): CTA b takes group g = b mod G of
+// tokens [tile Q, tile Q + Q), tile = b / G, so the eight quads of a warp
+// write the scales of eight consecutive tokens of one group, one 32-byte
+// sector of column-major scales instead of eight; the CTAs that follow read
+// the same Q rows' next groups.  Grid: ceil(T G / Q) CTAs flat,
+// ceil(T / Q) G token-major.  Measured, op A at T = 4096, H = 7168: UE8M0
+// column-major scales 15.62 us flat, 14.95 us token-major (used there); fp32
+// column-major 15.5 flat, 15.8 token-major; op C with exponent-byte scales
+// 80.9-81.6 flat, 85.9-86.1 token-major (flat kept): reading eight rows per
+// warp instead of one contiguous run costs the heavier kernels more than the
+// scattered scale stores.
+template <bool TOKEN_MAJOR, int Q>
+__device__ __forceinline__ bool group_of(uint32_t b, int quad, int64_t G, int64_t T, int64_t &t, int64_t &g)
+{
+    if (!TOKEN_MAJOR) {
+        const int64_t n = T * G, gi = int64_t(b) * Q + quad;
+        split_group(gi < n ? gi : n - 1, G, t, g);
+        return gi < n;
+    }
+    const uint32_t tile = b / uint32_t(G);
+    g = int64_t(b) - int64_t(tile) * G;
+    t = int64_t(tile) * Q + quad;
+    const bool ok = t < T;
+    if (!ok)
+        t = T - 1;
+    return ok;
+}
+
 // --------------------------------------------------------------------------
 // per_token_group_fp8_quant
 //
 // A contiguous [T, H] tensor is a flat sequence of T*G groups, so the kernel
-// walks groups, not rows.  CTA b owns groups [b*32*GPT, (b+1)*32*GPT); quad q
-// of the CTA takes groups b*32*GPT + j*32 + q for j < GPT, so the 8 quads of
-// a warp read 8 adjacent groups (2 KiB) per pair of load instructions.
-// Out-of-range quads load a clamped, valid group and store nothing.
+// walks groups, not rows (group_of: the flat order, or token-major tiles for
+// UE8M0 column-major scales).  One group per quad, 32 per CTA; every
+// lane issues its 64-byte load before any arithmetic.  Out-of-range quads
+// load a valid group and store nothing.
 // --------------------------------------------------------------------------
 template <bool UE8M0, int LAYOUT, bool V8>
 __global__ void __launch_bounds__(kGroupCtaThreads) group_quant_kernel(const uint16_t *__restrict__ x,
                                                                   uint8_t *__restrict__ q,
                                                                   float *__restrict__ scales,
-                                                                  int64_t n_groups, int64_t G,
-                                                                  int64_t T, float eps)
+                                                                  int64_t G, int64_t T, float eps)
 {
-    constexpr int GPT = kGroupQuantGpt;
     const int sub = threadIdx.x & (kLanesPerGroup - 1);
-    const int64_t first = int64_t(blockIdx.x) * kGroupQuantGroupsPerCta * GPT + (threadIdx.x / kLanesPerGroup);
+    int64_t t, g;
+    const bool ok = group_of<kGroupTokenMajor<UE8M0, LAYOUT>, kGroupQuantGroupsPerCta>(
+        blockIdx.x, threadIdx.x / kLanesPerGroup, G, T, t, g);
+    const int64_t off = (t * G + g) * kGroup + sub * kValsPerLane;
 
     wait_for_producer();
     allow_consumer_launch();
-    uint32_t raw[GPT][16];
+    uint32_t raw[16];
+    ld64_stream<V8>(x + off, raw);
+    uint64_t v[16];
+    float m = 0.0f;
 #pragma unroll
-    for (int j = 0; j < GPT; ++j) {
-        const int64_t gi = first + int64_t(j) * kGroupQuantGroupsPerCta;
-        const int64_t gl = gi < n_groups ? gi : n_groups - 1;
-        ld64_stream<V8>(x + gl * kGroup + sub * kValsPerLane, raw[j]);
+    for (int k = 0; k < 16; ++k) {
+        v[k] = f2_from_bf16x2(raw[k]);
+        m = absmax3(m, bf_lo(raw[k]), bf_hi(raw[k]));
     }
+    const float amax = quad_max(m);
+    const float s = group_scale<UE8M0>(amax, eps);
+    const float r = scale_recip<UE8M0>(s);
+    uint32_t codes[8];
 #pragma unroll
-    for (int j = 0; j < GPT; ++j) {
-        const int64_t gi = first + int64_t(j) * kGroupQuantGroupsPerCta;
-        uint64_t v[16];
-        float m = 0.0f;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            v[k] = f2_from_bf16x2(raw[j][k]);
-            m = absmax3(m, bf_lo(raw[j][k]), bf_hi(raw[j][k]));
-        }
-        const float amax = quad_max(m);
-        const float s = group_scale<UE8M0>(amax, eps);
-        const float r = scale_recip<UE8M0>(s);
-        uint32_t codes[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            quant8<UE8M0>(*reinterpret_cast<const uint64_t(*)[4]>(&v[4 * i]), s, r, codes[2 * i],
-                          codes[2 * i + 1]);
-        if (gi < n_groups) {
-            st32<V8>(q + gi * kGroup + sub * kValsPerLane, codes);
-            if (sub == 0) {
-                int64_t t, g;
-                split_group(gi, G, t, g);
-                store_scale<LAYOUT>(scales, s, t, g, T, G);
-            }
-        }
+    for (int i = 0; i < 4; ++i)
+        quant8<UE8M0>(*reinterpret_cast<const uint64_t(*)[4]>(&v[4 * i]), s, r, codes[2 * i], codes[2 * i + 1]);
+    if (ok) {
+        st32<V8>(q + off, codes);
+        if (sub == 0)
+            store_scale<LAYOUT>(scales, s, t, g, T, G);
     }
 }
 
@@ -181,14 +203,12 @@ template <bool UE8M0, int LAYOUT, bool V8>
 __global__ void __launch_bounds__(kSiluCtaThreads, 16) silu_quant_kernel(const uint16_t *__restrict__ x,
                                                                  uint8_t *__restrict__ q,
                                                                  float *__restrict__ scales,
-                                                                 int64_t n_groups, int64_t G,
-                                                                 int64_t T, int64_t I, float eps)
+                                                                 int64_t G, int64_t T, int64_t I, float eps)
 {
     const int sub = threadIdx.x & (kLanesPerGroup - 1);
-    const int64_t gi = int64_t(blockIdx.x) * kSiluGroupsPerCta + (threadIdx.x / kLanesPerGroup);
-    const int64_t gl = gi < n_groups ? gi : n_groups - 1;
     int64_t t, g;
-    split_group(gl, G, t, g);
+    const bool ok = group_of<false, kSiluGroupsPerCta>(blockIdx.x, threadIdx.x / kLanesPerGroup, G, T, t, g);
+    const int64_t gi = t * G + g;
     const uint16_t *pa = x + t * 2 * I + g * kGroup + sub * kValsPerLane;
     wait_for_producer();
     allow_consumer_launch();
@@ -212,7 +232,7 @@ __global__ void __launch_bounds__(kSiluCtaThreads, 16) silu_quant_kernel(const u
 #pragma unroll
     for (int i = 0; i < 4; ++i)
         quant8<UE8M0>(*reinterpret_cast<const uint64_t(*)[4]>(&v[4 * i]), s, r, codes[2 * i], codes[2 * i + 1]);
-    if (gi < n_groups) {
+    if (ok) {
         st32<V8>(q + gi * kGroup + sub * kValsPerLane, codes);
         if (sub == 0)
             store_scale<LAYOUT>(scales, s, t, g, T, G);
