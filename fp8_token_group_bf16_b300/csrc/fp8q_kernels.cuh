@@ -1,17 +1,19 @@
-// The three quantisation kernels for sm_103a.
+// The per-group quantisation kernels of ops A and C for sm_103a, the SiLU
+// arithmetic they share with the per-token kernels, and two small kernels
+// that expose single steps for checking (the e4m3 rounding, the SiLU value).
 //
-// All three are HBM-bound streaming kernels: a handful of fp32 operations per
+// They are HBM-bound streaming kernels: a handful of fp32 operations per
 // byte moved, no contraction, so no tensor cores.  A quad of lanes owns a
-// group (32 values per lane); every lane issues all of its loads before any
-// arithmetic so several 64-byte requests per thread are in flight.
+// group (32 values per lane); every lane issues all of its loads (64 bytes,
+// or 2 x 64 bytes of gate and up) before any arithmetic.
 #pragma once
 
 #include "fp8q_device.cuh"
 
 namespace fp8q {
 
-constexpr int kCtaThreads = 256;                               // ops A and C
-constexpr int kGroupsPerCta = kCtaThreads / kLanesPerGroup;    // 64
+constexpr int kCtaThreads = 256;                               // largest CTA of the per-token kernels
+constexpr int kGroupsPerCta = kCtaThreads / kLanesPerGroup;    // 64 groups
 // Op A in CTAs of four warps, one group per quad (32 groups per CTA).
 // Measured (UE8M0 column-major / fp32 row-major scales, H = 7168): T = 4096
 // 15.45 / 15.01 us, T = 16384 54.3 / 53.4 us, T = 512 3.28 / 3.89 us;
