@@ -244,3 +244,28 @@ def test_widened_ops_in_a_graph():
         e8 = e.view(torch.uint8) if e.dtype == torch.float8_e4m3fn else e
         o8 = o.view(torch.uint8) if o.dtype == torch.float8_e4m3fn else o
         assert torch.equal(e8, o8)
+
+
+def test_tensor_api_rejects_wrong_scale_buffers():
+    """The tensor-level calls check caller-provided scale buffers against the
+    layout before anything is launched."""
+    x = torch.zeros(5, 640, dtype=torch.bfloat16, device="cuda")
+    G = 5
+    with pytest.raises(ValueError):   # packed words need [ceil(G/4), T rounded up to 4]
+        fq.per_token_group_fp8_quant(x, ue8m0=True, packed_ue8m0_scales=True,
+                                     scales=torch.empty(2, 5, dtype=torch.int32, device="cuda"))
+    with pytest.raises(ValueError):   # MXFP8 tiles need [T rounded up to 128, 4 G] bytes
+        fq.per_token_group_fp8_quant(x, ue8m0=True, mx_scales=True,
+                                     scales=torch.empty(5, 4 * G, dtype=torch.uint8, device="cuda"))
+    with pytest.raises(ValueError):   # row-major fp32 [T, G]
+        fq.per_token_group_fp8_quant(x, scales=torch.empty(5, G + 1, device="cuda"))
+    with pytest.raises(ValueError):   # column-major: a [T, G] view of a [G, T] buffer, not a [T, G] buffer
+        fq.per_token_group_fp8_quant(x[:, :512].contiguous(), column_major_scales=True,
+                                     scales=torch.empty(5, 4, device="cuda"))
+    with pytest.raises(ValueError):   # per-token scales: T values
+        fq.dynamic_per_token_scaled_fp8_quant(x, scales=torch.empty(4, device="cuda"))
+    # the right shapes go through
+    q, s = fq.per_token_group_fp8_quant(x, ue8m0=True, mx_scales=True,
+                                        scales=torch.empty(fq.mx_scale_shape(5, G), dtype=torch.uint8, device="cuda"))
+    torch.cuda.synchronize()
+    assert s.shape == (128, 4 * G)
