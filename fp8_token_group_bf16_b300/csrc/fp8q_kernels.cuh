@@ -27,10 +27,11 @@ template <bool UE8M0, int LAYOUT>
 constexpr bool kGroupTokenMajor = UE8M0 && LAYOUT == kColMajor;
 constexpr int kGroupQuantGroupsPerCta = kGroupCtaThreads / kLanesPerGroup;   // 32
 // Op C in CTAs of two warps (16 groups): 64 registers a thread allow 16 such
-// CTAs per SM.  Measured at T = 4096, I = 25600: 82.8 us, against 83.4 us
-// with 128-thread and 85.9 us with 256-thread CTAs (the same 32 warps per SM
-// in all three; smaller CTAs retire and refill independently), and 106 us
-// with one-warp CTAs (the 32-CTAs-per-SM limit leaves the SM half empty).
+// CTAs per SM.  Measured at T = 4096, I = 25600 (with CUDA's expf then):
+// 82.8 us, against 83.4 us with 128-thread and 85.9 us with 256-thread CTAs
+// (the same 32 warps per SM in all three; smaller CTAs retire and refill
+// independently), and 106 us with one-warp CTAs (102,400 CTAs at about 970
+// per us: the CTA launch rate limits).
 constexpr int kSiluCtaThreads = 64;
 constexpr int kSiluGroupsPerCta = kSiluCtaThreads / kLanesPerGroup;   // 16
 
