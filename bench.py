@@ -799,7 +799,7 @@ def single_op(args):
         table = _inputs.rotary_table(_inputs.QK_P).to(dev)
         w = (1.0 + 0.1 * torch.randn(128, device=dev)).to(torch.bfloat16)
     else:
-        nbytes = algorithmic_bytes(op, T, H, packed=args.packed)
+        nbytes = algorithmic_bytes(op, T, H, packed=args.packed, mx=args.mx)
     nsets = min(16, max(2, int(3 * (126 << 20) // nbytes) + 1))
     calls = []
     for _ in range(nsets):
@@ -818,8 +818,9 @@ def single_op(args):
             else:
                 calls.append(lambda x=x, q=q, f=f: f(x, q=q))
             continue
-        kw = dict(ue8m0=ue8m0 or args.packed, column_major_scales=lay == "col" and not args.packed,
-                  packed_ue8m0_scales=args.packed, q=q)
+        kw = dict(ue8m0=ue8m0 or args.packed or args.mx,
+                  column_major_scales=lay == "col" and not (args.packed or args.mx),
+                  packed_ue8m0_scales=args.packed, mx_scales=args.mx, q=q)
         if op.startswith("rms"):
             wt = torch.randn(H, device=dev).to(torch.bfloat16)
             calls.append(lambda x=x, wt=wt, kw=kw: fq.rms_norm_per_block_quant(x, wt, None, **kw))
@@ -837,7 +838,7 @@ def single_op(args):
     torch.cuda.synchronize()
     us = a.elapsed_time(b) * 1e3 / args.steps
     peak, kind = load_peaks()
-    print(json.dumps({"op": op, "T": T, "packed": args.packed, "launches": args.steps, "us": round(us, 3),
+    print(json.dumps({"op": op, "T": T, "packed": args.packed, "mx": args.mx, "launches": args.steps, "us": round(us, 3),
                       "GBps": round(nbytes / us / 1e3, 1), "frac_of_peak": round(nbytes / us / 1e3 / peak, 4),
                       "peak": peak, "peak_kind": kind}), flush=True)
 
@@ -856,6 +857,7 @@ def parse_args(argv=None):
     p.add_argument("--op", choices=sorted(SINGLE_OPS), default=None,
                    help="time one op at --tokens (K launches after W warm-ups) instead of the step")
     p.add_argument("--packed", action="store_true", help="with --op: packed UE8M0 scales (per-group ops)")
+    p.add_argument("--mx", action="store_true", help="with --op: MXFP8 scale tiles (per-group ops)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--tokens", type=int, default=STEP_T,
                    help="tokens per step (default: the T=4096 workload; smaller values are for profiling)")
