@@ -6,6 +6,8 @@
 #include "fp8q_rope.cuh"
 #include "fp8q_token.cuh"
 
+#include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -59,6 +61,33 @@ int launch_status(cudaError_t launched)
 {
     const cudaError_t last = cudaGetLastError();
     return (launched == cudaSuccess && last == cudaSuccess) ? FP8Q_OK : FP8Q_ERR_CUDA;
+}
+
+// SM count of the current device, cached per device.  It only sets prefetch
+// distances (never a grid or an index); a failed query reads as 0 (no
+// prefetch) and leaves its error for the launch status to report.
+int sm_count()
+{
+    static std::atomic<int> cache[32];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 0;
+    const bool keep = dev >= 0 && dev < 32;
+    int n = keep ? cache[dev].load(std::memory_order_relaxed) : 0;
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 0)
+            return 0;
+        if (keep)
+            cache[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
+// CTAs of `threads` threads at up to `regs` registers a thread that one SM
+// holds at once (its 2048 threads, 65536 registers and 32 CTAs).
+int resident_per_sm(int threads, int regs)
+{
+    return std::min({32, 2048 / threads, 65536 / (regs * threads)});
 }
 
 // Launch with programmatic stream serialization allowed: the kernel may be
@@ -130,8 +159,17 @@ cudaError_t launch_rms_row(const uint16_t *x, uint16_t *res, const uint16_t *w, 
 {
     const int quads = (G + NG - 1) / NG;
     const int threads = ((quads * 4 + 31) / 32) * 32;
-    return launch(rms_row_kernel<NG, U, C, R, V>, dim3{unsigned(T)}, dim3{unsigned(threads)}, st, x, res, w, q, s,
-                  T, H, G, eps);
+    const dim3 grid{unsigned(T)}, block{unsigned(threads)};
+    // The prefetching build, at a distance of 1.5 x the SM count, when rows
+    // wait for a later wave (more rows than CTAs resident at once), without
+    // the residual.
+    if constexpr (!R) {
+        const int sms = sm_count();
+        if (int64_t(T) > int64_t(sms) * resident_per_sm(threads, 65536 / (kRmsMaxThreads * kRmsMinCtas<NG>)))
+            return launch(rms_row_kernel<NG, U, C, R, V, true>, grid, block, st, x, res, w, q, s, T, H, G, eps,
+                          sms * 3 / 2);
+    }
+    return launch(rms_row_kernel<NG, U, C, R, V, false>, grid, block, st, x, res, w, q, s, T, H, G, eps, 0);
 }
 
 template <bool U, int C, bool R>
@@ -184,14 +222,21 @@ int launch_token(const uint16_t *x, uint8_t *q, float *s, int64_t T, int64_t col
     const dim3 grid{unsigned(T * C)}, block{unsigned(threads)};
     const int c = int(cols);
     cudaError_t e;
-#define FP8Q_TOKEN(U, V)                                                                         \
-    launch_ex(SILU ? token_silu_kernel<U, V> : token_quant_kernel<U, V>, grid, block, unsigned(C), 0, st, x, q, s, \
-              c, G, gpc, C, eps)
+    // The prefetching builds, at a distance of 3 x the SM count, when CTAs
+    // wait for a later wave (more CTAs than resident at once).
+    const int sms = sm_count();
+    const int regs = 65536 / (kCtaThreads * (SILU ? kTokenSiluMinCtas : kTokenQuantMinCtas));
+    const int pf = T * C > int64_t(sms) * resident_per_sm(threads, regs) ? 3 * sms : 0;
+#define FP8Q_TOKEN_PF(K, U, V, PF) launch_ex(K<U, V, PF>, grid, block, unsigned(C), 0, st, x, q, s, c, G, gpc, C, eps, pf)
+#define FP8Q_TOKEN_K(K, U, V) (pf > 0 ? FP8Q_TOKEN_PF(K, U, V, true) : FP8Q_TOKEN_PF(K, U, V, false))
+#define FP8Q_TOKEN(U, V) (SILU ? FP8Q_TOKEN_K(token_silu_kernel, U, V) : FP8Q_TOKEN_K(token_quant_kernel, U, V))
     if (ue8m0)
         e = v8 ? FP8Q_TOKEN(true, true) : FP8Q_TOKEN(true, false);
     else
         e = v8 ? FP8Q_TOKEN(false, true) : FP8Q_TOKEN(false, false);
 #undef FP8Q_TOKEN
+#undef FP8Q_TOKEN_K
+#undef FP8Q_TOKEN_PF
     return launch_status(e);
 }
 

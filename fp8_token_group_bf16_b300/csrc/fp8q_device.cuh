@@ -164,6 +164,21 @@ __device__ __forceinline__ void allow_consumer_launch()
 #endif
 }
 
+// Ask the L2 to fetch `bytes` (a multiple of 16) starting at the 16-byte
+// aligned global address p, in bulk requests of at most 8 KiB.  A hint: it
+// returns at once, holds no registers and changes no result.  Kernels whose
+// CTAs wait on a barrier use it to fetch the input of a CTA that starts
+// later, so that HBM keeps streaming while the resident CTAs wait.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes)
+{
+    constexpr uint32_t kChunk = 8192;
+    const char *c = static_cast<const char *>(p);
+    for (uint32_t o = 0; o < bytes; o += kChunk) {
+        const uint32_t n = bytes - o < kChunk ? bytes - o : kChunk;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c + o), "r"(n) : "memory");
+    }
+}
+
 // --------------------------------------------------------------- bf16 ---
 
 // bf16 -> fp32 is exact: the bf16 bits are the top half of the fp32 bits.

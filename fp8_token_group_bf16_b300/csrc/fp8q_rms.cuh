@@ -20,6 +20,10 @@
 namespace fp8q {
 
 constexpr int kRmsMaxThreads = 256;
+// CTAs per SM the launch bounds ask for (and so the register cap): NG groups
+// per quad hold 32 NG values and as many weights in registers.
+template <int NG>
+constexpr int kRmsMinCtas = NG == 1 ? 4 : (NG == 2 ? 2 : 1);
 
 // Squares of one lane's 2*NW values (NW bf16x2 words, NW even), summed
 // exactly: returns (hi, lo) with hi + lo equal to the sum up to lo's own
@@ -80,16 +84,26 @@ __device__ __forceinline__ float rms_inv(float hi, float lo, int H, float eps)
 // the same bytes).  Short-lived CTAs at ~64 registers leave room for six per
 // SM, whose loads overlap the others' arithmetic.
 //
+// While a CTA waits on its barrier, its loads are done and it asks nothing of
+// HBM.  When the grid is longer than the CTAs resident at once, the PF
+// variant therefore has thread 0 hand row + pf to the L2 once its own loads
+// are issued (pf = 1.5 x the SM count, set by the host): 14.3 us against
+// 15.05 us at T = 4096, H = 5120, 48.1 against 52.1 us at T = 16384; per
+// token 69.9 against 71.4 us at T = 16384.  The other launches run a build
+// without that code, whose mere presence cost 2-5 % in single-wave grids
+// (T <= 512), and which measured slower with the residual (24.7 against
+// 23.95 us at T = 4096, the residual row prefetched too).
+//
 // LAYOUT == kPerToken is rms_norm_dynamic_per_token_quant: one scale for the
 // whole row.  The normalised values are then formed twice from the registers
 // (once for the row maximum, joined across warps by a second barrier, once to
 // quantise), which is two multiplies per pair of values instead of keeping
 // another 32 registers per group alive.
 
-template <int NG, bool UE8M0, int LAYOUT, bool RES, bool V8>
-__global__ void __launch_bounds__(kRmsMaxThreads, NG == 1 ? 4 : (NG == 2 ? 2 : 1)) rms_row_kernel(
+template <int NG, bool UE8M0, int LAYOUT, bool RES, bool V8, bool PF>
+__global__ void __launch_bounds__(kRmsMaxThreads, kRmsMinCtas<NG>) rms_row_kernel(
     const uint16_t *__restrict__ x, uint16_t *__restrict__ residual, const uint16_t *__restrict__ w,
-    uint8_t *__restrict__ q, float *__restrict__ scales, int T, int H, int G, float eps)
+    uint8_t *__restrict__ q, float *__restrict__ scales, int T, int H, int G, float eps, int pf)
 {
     __shared__ float2 red[kRmsMaxThreads / 32];
     __shared__ float redm[kRmsMaxThreads / 32];
@@ -115,6 +129,13 @@ __global__ void __launch_bounds__(kRmsMaxThreads, NG == 1 ? 4 : (NG == 2 ? 2 : 1
                 z[j][e] = pack_bf16x2(__fadd_rn(bf_lo(z[j][e]), bf_lo(r[e])), __fadd_rn(bf_hi(z[j][e]), bf_hi(r[e])));
         }
         ld64_keep_l1<V8>(w + off, wr[j]);
+    }
+    // With this CTA's loads issued, row row + pf into L2 for the CTA that
+    // will take it.
+    if constexpr (PF) {
+        static_assert(!RES, "no prefetch with the residual");
+        if (tid == 0 && row + pf < T)
+            prefetch_l2_bulk(x + rbase + int64_t(pf) * H, uint32_t(H) * 2);
     }
     if (RES) {
 #pragma unroll

@@ -117,12 +117,15 @@ __device__ __forceinline__ float row_max_exchange(float m, float *part, int rank
 // lane stay live across the row exchange (the maximum of |x| is taken on the
 // bf16 values, which is exact); the fp32 values are formed afterwards, as in
 // the per-group kernel, which keeps the register count at the per-group
-// kernel's.
-template <bool UE8M0, bool V8>
-__global__ void __launch_bounds__(kCtaThreads, 5) token_quant_kernel(const uint16_t *__restrict__ x,
-                                                                   uint8_t *__restrict__ q,
-                                                                   float *__restrict__ scales, int cols,
-                                                                   int G, int gpc, int C, float eps)
+// kernel's.  The PF build prefetches like token_silu_kernel below (3 x the
+// SM count ahead, issued after the CTA's own loads): 16.8 us against 18.1 us
+// at T = 4096, H = 7168, 56.7 against 64.8 us at T = 16384.
+constexpr int kTokenQuantMinCtas = 5;   // per SM, at 256 threads: 51 registers
+
+template <bool UE8M0, bool V8, bool PF>
+__global__ void __launch_bounds__(kCtaThreads, kTokenQuantMinCtas) token_quant_kernel(
+    const uint16_t *__restrict__ x, uint8_t *__restrict__ q, float *__restrict__ scales, int cols, int G, int gpc,
+    int C, float eps, int pf)
 {
     __shared__ float part[kTokenMaxCluster * kTokenMaxWarps];
     const int tid = threadIdx.x, sub = tid & 3, quad = tid >> 2;
@@ -138,6 +141,12 @@ __global__ void __launch_bounds__(kCtaThreads, 5) token_quant_kernel(const uint1
 
     uint32_t raw[16];
     ld64_stream<V8>(x + off, raw);
+    // With this CTA's loads issued, the input of CTA blockIdx.x + pf into L2.
+    if (PF && tid == 0 && int64_t(blockIdx.x) + pf < int64_t(gridDim.x)) {
+        const int bp = int(blockIdx.x) + pf, rp = bp / C, gp = (bp - rp * C) * gpc;
+        const uint32_t bytes = uint32_t(G - gp < gpc ? G - gp : gpc) * kGroup * 2;
+        prefetch_l2_bulk(x + int64_t(rp) * cols + int64_t(gp) * kGroup, bytes);
+    }
     float m = 0.0f;
 #pragma unroll
     for (int k = 0; k < 16; ++k)
@@ -165,11 +174,22 @@ __global__ void __launch_bounds__(kCtaThreads, 5) token_quant_kernel(const uint1
 // registers across the exchange.  Staging the inputs in shared memory with
 // cp.async instead, to free those registers for more CTAs per SM, measured
 // slower (174 us against 142 us at T = 4096, I = 25600).
-template <bool UE8M0, bool V8>
-__global__ void __launch_bounds__(kCtaThreads, 4) token_silu_kernel(const uint16_t *__restrict__ x,
+//
+// While a cluster's warps wait on its barrier their loads are done, so in
+// the PF build (launched when CTAs wait for a later wave) thread 0 hands the
+// input of CTA blockIdx.x + pf to the L2 once its own loads are issued
+// (pf = 3 x the SM count, set by the host; about half the CTAs resident at
+// once), and that CTA then finds its bytes there: 105.9 us against 123.5 us
+// at T = 4096, I = 25600 (fp32 scales), 30.6 against 34.5 us at T = 1024.  Issued before
+// the CTA's own loads it gained less (109.5 us); distances of 1, 2 and 4 x
+// the SM count measured within 3 % of 3 x.
+constexpr int kTokenSiluMinCtas = 4;   // per SM, at 256 threads: 64 registers
+
+template <bool UE8M0, bool V8, bool PF>
+__global__ void __launch_bounds__(kCtaThreads, kTokenSiluMinCtas) token_silu_kernel(const uint16_t *__restrict__ x,
                                                                   uint8_t *__restrict__ q,
                                                                   float *__restrict__ scales, int cols,
-                                                                  int G, int gpc, int C, float eps)
+                                                                  int G, int gpc, int C, float eps, int pf)
 {
     __shared__ float part[kTokenMaxCluster * kTokenMaxWarps];
     const int tid = threadIdx.x, sub = tid & 3, quad = tid >> 2;
@@ -187,6 +207,15 @@ __global__ void __launch_bounds__(kCtaThreads, 4) token_silu_kernel(const uint16
     uint32_t ra[16], rb[16];
     ld64_stream<V8>(pa, ra);
     ld64_stream<V8>(pa + cols, rb);
+    // With this CTA's loads issued, the gate and up segments of CTA
+    // blockIdx.x + pf into L2.
+    if (PF && tid == 0 && int64_t(blockIdx.x) + pf < int64_t(gridDim.x)) {
+        const int bp = int(blockIdx.x) + pf, rp = bp / C, gp = (bp - rp * C) * gpc;
+        const uint32_t bytes = uint32_t(G - gp < gpc ? G - gp : gpc) * kGroup * 2;
+        const uint16_t *pp = x + int64_t(rp) * 2 * cols + int64_t(gp) * kGroup;
+        prefetch_l2_bulk(pp, bytes);
+        prefetch_l2_bulk(pp + cols, bytes);
+    }
     uint64_t v[16];
     float m = 0.0f;
 #pragma unroll

@@ -20,7 +20,10 @@ from tolerance import check_fused
 
 pytestmark = pytest.mark.gpu
 
-A_SHAPES = [(1, 128), (7, 896), (37, 7168), (3, 8192), (5, 8320), (4, 25600), (2, 65536), (1024, 5120)]
+# The last two are longer than one wave of CTAs, which launches the build
+# that prefetches a later CTA's input into L2.
+A_SHAPES = [(1, 128), (7, 896), (37, 7168), (3, 8192), (5, 8320), (4, 25600), (2, 65536), (1024, 5120),
+            (2048, 7168), (256, 25600)]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -120,7 +123,7 @@ def _token_rms(xb, wb, rb, ue8m0):
 
 @pytest.mark.parametrize("T,H,residual", [(1, 128, False), (7, 896, True), (256, 4096, False),
                                           (256, 4096, True), (3, 24576, False), (2, 32768, True),
-                                          (5, 16384, False), (512, 5120, True)])
+                                          (5, 16384, False), (512, 5120, True), (2048, 5120, False)])
 @pytest.mark.parametrize("ue8m0", [False, True], ids=["fp32", "ue8m0"])
 def test_rms_per_token_exact(T, H, residual, ue8m0):
     x, w, r = inputs.rms_input(T, H, seeds=(5300 + T, 5301 + H, 5302))
@@ -155,7 +158,7 @@ def _check_token_silu(xb, ue8m0, what):
 
 
 @pytest.mark.parametrize("T,I", [(1, 128), (7, 896), (37, 1152), (64, 12288), (5, 8320), (4, 25600),
-                                 (2, 65536)])
+                                 (2, 65536), (512, 25600)])
 @pytest.mark.parametrize("ue8m0", [False, True], ids=["fp32", "ue8m0"])
 def test_silu_per_token(T, I, ue8m0):
     xb = inputs.bits(inputs.silu_input(T, I, seed=5500 + T + I))
