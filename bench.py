@@ -15,7 +15,9 @@ once, every output written once) divided by time.  Rank 0 prints one JSON
 line.  ``value`` is device-timed with the inputs already in HBM; ``e2e`` is
 the same metric through the package's public calls with the inputs copied
 from pinned host memory and the outputs copied back inside the timed
-region; ``roofline`` is the dominant kernel's bandwidth (CUDA events around
+region, with ``e2e.host_link`` the link's own rate for the same bytes
+(plain copies, each direction alone and both at once) as its ceiling;
+``roofline`` is the dominant kernel's bandwidth (CUDA events around
 its launches) against the measured copy bandwidth; ``cpu_baseline`` is the
 CPU oracle timed on a bounded sample.  Under torchrun every rank processes
 its own batch (weak scaling, no collective on the data path).
@@ -526,6 +528,44 @@ class E2EPipeline:
         self.prev_c_done, self.prev_out = c_done, ev_out
 
 
+def host_link_ceiling(h2d_bytes: int, d2h_bytes: int, reps: int = 5) -> dict:
+    """The host link's own rate for one step's bytes: plain copies of
+    h2d_bytes from pinned host memory and d2h_bytes back, each alone and both
+    at once on two streams (median of `reps` after one warm-up, host wall
+    clock).  No kernel runs; it is the ceiling the end-to-end number is
+    read against."""
+    import torch
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    hin = torch.empty(h2d_bytes, dtype=torch.uint8, pin_memory=True)
+    hout = torch.empty(d2h_bytes, dtype=torch.uint8, pin_memory=True)
+    din = torch.empty(h2d_bytes, dtype=torch.uint8, device=dev)
+    dout = torch.zeros(d2h_bytes, dtype=torch.uint8, device=dev)
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def once(h2d: bool, d2h: bool) -> float:
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        if h2d:
+            with torch.cuda.stream(s_in):
+                din.copy_(hin, non_blocking=True)
+        if d2h:
+            with torch.cuda.stream(s_out):
+                hout.copy_(dout, non_blocking=True)
+        torch.cuda.synchronize()
+        return time.perf_counter() - t0
+
+    def rate(h2d: bool, d2h: bool) -> float:
+        once(h2d, d2h)
+        secs = statistics.median(once(h2d, d2h) for _ in range(reps))
+        return ((h2d_bytes if h2d else 0) + (d2h_bytes if d2h else 0)) / secs / 1e9
+
+    out = {"h2d_alone_GBps": round(rate(True, False), 1), "d2h_alone_GBps": round(rate(False, True), 1),
+           "both_GBps": round(rate(True, True), 1)}
+    del hin, hout, din, dout
+    return out
+
+
 def time_e2e(host, steps: int, dist: Dist, chunks: int = 8):
     """The end-to-end metric: `steps` pipelined steps (E2EPipeline) between
     two synchronisations, host wall clock, max over ranks."""
@@ -543,9 +583,12 @@ def time_e2e(host, steps: int, dist: Dist, chunks: int = 8):
     secs = time.perf_counter() - t0
     dist.barrier()
     agg = aggregate(step_bytes(pipe.T) * steps, secs, dist, steps)
+    link = host_link_ceiling(pipe.h2d, pipe.d2h)
+    link["frac"] = round((pipe.h2d + pipe.d2h) / (agg["ms_per_step"] * 1e-3) / 1e9 / link["both_GBps"], 4)
     return {"value": round(agg["value"], 2), "unit": UNIT, "h2d_bytes_per_step": pipe.h2d,
             "d2h_bytes_per_step": pipe.d2h, "steps": steps, "ms_per_step": round(agg["ms_per_step"], 3),
-            "pipeline": f"{len(pipe.bounds)} token slices, copy-in / compute / copy-out streams"}
+            "pipeline": f"{len(pipe.bounds)} token slices, copy-in / compute / copy-out streams",
+            "host_link": link}
 
 
 # ------------------------------------------------------------ CPU oracle ---

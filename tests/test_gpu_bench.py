@@ -43,3 +43,17 @@ def test_e2e_pipeline_outputs(T, chunks):
         assert torch.equal(psb, sb.cpu()[lo:hi])
         assert torch.equal(pqc.view(torch.uint8), u8(qc)[lo:hi])
         assert torch.equal(psc, sc.cpu()[lo:hi])
+
+
+def test_e2e_record_carries_its_host_link_ceiling():
+    """time_e2e reports the step's host bytes and, beside them, the host
+    link's own rate for those bytes; the pipelined step cannot beat a plain
+    copy of the same bytes by more than timing noise."""
+    host = bench.workload_inputs(64)
+    rec = bench.time_e2e(host, 3, bench.Dist())
+    inputs = (host["per_token_group_fp8_quant"][0], *host["rms_norm_per_block_quant"][:2],
+              host["silu_and_mul_per_block_quant"][0])
+    assert rec["h2d_bytes_per_step"] == sum(t.numel() * t.element_size() for t in inputs)
+    link = rec["host_link"]
+    assert min(link["h2d_alone_GBps"], link["d2h_alone_GBps"], link["both_GBps"]) > 0
+    assert 0 < link["frac"] < 1.5
