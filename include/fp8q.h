@@ -28,8 +28,9 @@
  *
  * Conventions shared by every entry point:
  *  - Pointers are DEVICE pointers (global memory of the current device).  The
- *    caller owns and allocates every buffer; the library allocates nothing
- *    and keeps no state between calls.
+ *    caller owns and allocates every buffer; the library allocates nothing.
+ *    Its only state between calls is a per-device cache of the SM count,
+ *    which chooses launch variants and never changes a result.
  *  - bf16 tensors are row-major and contiguous (row stride = row length);
  *    `q` is float8_e4m3fn bytes, row-major [T, H] (or [T, I]).
  *  - `x`, `q`, `residual` and `weight` must be 16-byte aligned, `scales`
