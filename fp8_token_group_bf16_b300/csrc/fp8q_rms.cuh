@@ -95,10 +95,11 @@ __device__ __forceinline__ float rms_inv(float hi, float lo, int H, float eps)
 // 23.95 us at T = 4096, the residual row prefetched too).
 //
 // LAYOUT == kPerToken is rms_norm_dynamic_per_token_quant: one scale for the
-// whole row.  The normalised values are then formed twice from the registers
-// (once for the row maximum, joined across warps by a second barrier, once to
-// quantise), which is two multiplies per pair of values instead of keeping
-// another 32 registers per group alive.
+// whole row.  The normalised values v are formed once, into the registers
+// that z and w free (32 a group either way), their row maximum is joined
+// across warps by a second barrier, and the codes are taken from v: 18.5 us
+// against 20.0 us at T = 4096, H = 5120 for forming v a second time from z
+// and w after the barrier.
 
 template <int NG, bool UE8M0, int LAYOUT, bool RES, bool V8, bool PF>
 __global__ void __launch_bounds__(kRmsMaxThreads, kRmsMinCtas<NG>) rms_row_kernel(
@@ -168,17 +169,19 @@ __global__ void __launch_bounds__(kRmsMaxThreads, kRmsMinCtas<NG>) rms_row_kerne
     const uint64_t inv2 = f2_pack(inv, inv);
 
     if constexpr (LAYOUT == kPerToken) {
-        // ---- pass 2: row maximum of v = (z * inv) * w
+        // ---- pass 2: v = (z * inv) * w, in the registers z and w free, and its row maximum
+        uint64_t v[NG][16];
         float mm[2] = {0.0f, 0.0f};
 #pragma unroll
         for (int j = 0; j < NG; ++j) {
-            if (quad + nq * j < G) {
+            const bool act = quad + nq * j < G;
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    float va, vb;
-                    f2_unpack(f2_mul(f2_mul(f2_from_bf16x2(z[j][k]), inv2), f2_from_bf16x2(wr[j][k])), va, vb);
+            for (int k = 0; k < 16; ++k) {
+                v[j][k] = f2_mul(f2_mul(f2_from_bf16x2(z[j][k]), inv2), f2_from_bf16x2(wr[j][k]));
+                float va, vb;
+                f2_unpack(v[j][k], va, vb);
+                if (act)
                     mm[k & 1] = absmax3(mm[k & 1], va, vb);
-                }
             }
         }
         float m = fmaxf(mm[0], mm[1]);
@@ -194,20 +197,15 @@ __global__ void __launch_bounds__(kRmsMaxThreads, kRmsMinCtas<NG>) rms_row_kerne
         const float sc = group_scale<UE8M0>(amax, kScaleFloor);
         const float rc = scale_recip<UE8M0>(sc);
 
-        // ---- pass 3: the same values again, codes
+        // ---- pass 3: codes
 #pragma unroll
         for (int j = 0; j < NG; ++j) {
             const int g = quad + nq * j;
-            uint64_t v[4][4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    v[i][e] = f2_mul(f2_mul(f2_from_bf16x2(z[j][4 * i + e]), inv2), f2_from_bf16x2(wr[j][4 * i + e]));
             uint32_t codes[8];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                quant8<UE8M0>(v[i], sc, rc, codes[2 * i], codes[2 * i + 1]);
+                quant8<UE8M0>(*reinterpret_cast<const uint64_t(*)[4]>(&v[j][4 * i]), sc, rc, codes[2 * i],
+                              codes[2 * i + 1]);
             if (g < G)
                 st32<V8>(q + rbase + g * kGroup + sub * kValsPerLane, codes);
         }
