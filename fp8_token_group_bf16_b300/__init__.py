@@ -55,6 +55,7 @@ EXPORTS = (
     "fp8q_fused_qk_norm_rope",
     "fp8q_f32_to_e4m3",
     "fp8q_silu_mul",
+    "fp8q_group_scale",
     "fp8q_status_string",
     "fp8q_version",
 )
@@ -88,7 +89,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.fp8q_fused_qk_norm_rope.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, F, I32, P]
     L.fp8q_f32_to_e4m3.argtypes = [P, P, I64, P]
     L.fp8q_silu_mul.argtypes = [P, P, P, I64, P]
-    for n in EXPORTS[:9]:
+    L.fp8q_group_scale.argtypes = [P, P, I64, F, I32, P]
+    for n in EXPORTS[:10]:
         getattr(L, n).restype = ctypes.c_int
     L.fp8q_status_string.argtypes = [ctypes.c_int]
     L.fp8q_status_string.restype = ctypes.c_char_p
@@ -143,6 +145,10 @@ def fp8q_f32_to_e4m3(v, out, n, stream):
 
 def fp8q_silu_mul(a, b, out, n, stream):
     return load().fp8q_silu_mul(a, b, out, n, stream)
+
+
+def fp8q_group_scale(amax, scales, n, eps, ue8m0, stream):
+    return load().fp8q_group_scale(amax, scales, n, eps, ue8m0, stream)
 
 
 def fp8q_status_string(status: int) -> str:
@@ -406,6 +412,18 @@ def silu_mul(a, b, out=None, stream=None):
     if out is None:
         out = torch.empty_like(a)
     _check(fp8q_silu_mul(a.data_ptr(), b.data_ptr(), out.data_ptr(), a.numel(), _stream_ptr(a, stream)), "silu_mul")
+    return out
+
+
+def group_scale(amax, eps: float = 1e-10, ue8m0: bool = False, out=None, stream=None):
+    """fp32 CUDA tensor of group maxima -> the scales the kernels form from them."""
+    torch = _torch()
+    if amax.device.type != "cuda" or amax.dtype != torch.float32 or not amax.is_contiguous():
+        raise ValueError("amax must be a contiguous fp32 CUDA tensor")
+    if out is None:
+        out = torch.empty_like(amax)
+    _check(fp8q_group_scale(amax.data_ptr(), out.data_ptr(), amax.numel(), eps, int(ue8m0), _stream_ptr(amax, stream)),
+           "group_scale")
     return out
 
 

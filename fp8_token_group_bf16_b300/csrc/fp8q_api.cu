@@ -512,6 +512,27 @@ int fp8q_silu_mul(const float *a, const float *b, float *out, int64_t n, void *s
     return launch_status(cudaSuccess);
 }
 
+int fp8q_group_scale(const float *amax, float *scales, int64_t n, float eps, int32_t ue8m0, void *stream)
+{
+    if (n < 0 || !valid_scale_eps(eps))
+        return FP8Q_ERR_INVALID_ARG;
+    if (n == 0)
+        return FP8Q_OK;
+    if (!amax || !scales)
+        return FP8Q_ERR_INVALID_ARG;
+    if (!aligned(amax, 4) || !aligned(scales, 4))
+        return FP8Q_ERR_MISALIGNED;
+    const int64_t blocks = (n + 255) / 256;
+    if (blocks > 0x7FFFFFFF)
+        return FP8Q_ERR_UNSUPPORTED;
+    auto st = static_cast<cudaStream_t>(stream);
+    if (ue8m0)
+        group_scale_kernel<true><<<dim3{unsigned(blocks)}, 256, 0, st>>>(amax, scales, n, eps);
+    else
+        group_scale_kernel<false><<<dim3{unsigned(blocks)}, 256, 0, st>>>(amax, scales, n, eps);
+    return launch_status(cudaSuccess);
+}
+
 const char *fp8q_status_string(int status)
 {
     switch (status) {

@@ -12,6 +12,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "fp8q_rounding.cuh"
+
 namespace fp8q {
 
 constexpr int kGroup = 128;
@@ -269,10 +271,12 @@ __device__ __forceinline__ void store_scale(float *scales, float s, int64_t t, i
 // s = RN32(max(amax, eps) / 448); with UE8M0 the smallest power of two >= s.
 // eps >= 1e-30 (checked on the host) keeps s a normal number, so the power of
 // two is the exponent field bumped by one whenever any mantissa bit is set.
+// The division is div448_rn (two instructions, correctly rounded): it sits on
+// the path from a group's last value to its first code.
 template <bool UE8M0>
 __device__ __forceinline__ float group_scale(float amax, float eps)
 {
-    float s = __fdiv_rn(fmaxf(amax, eps), kFp8Max);
+    float s = div448_rn(fmaxf(amax, eps));
     if (UE8M0) {
         uint32_t u = __float_as_uint(s);
         if (u & 0x007FFFFFu)
@@ -355,6 +359,32 @@ __device__ __forceinline__ float absmax3(float m, float a, float b)
     float r;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(m), "f"(fabsf(a)), "f"(fabsf(b)));
     return r;
+}
+
+// Running magnitude maximum of bf16x2 words, one instruction per word: each
+// half of the result has the larger magnitude of the two halves in that
+// position (its sign bit is the xor of the operands' sign bits, which the
+// caller clears once at the end).  bf16 max keeps subnormals.
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t m, uint32_t w)
+{
+    uint32_t r;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(w));
+    return r;
+}
+
+// The largest |value| of NW bf16x2 words, as fp32 (exact).
+template <int NW>
+__device__ __forceinline__ float bf16x2_words_absmax(const uint32_t (&w)[NW])
+{
+    uint32_t m0 = 0, m1 = 0;
+#pragma unroll
+    for (int k = 0; k < NW; k += 2) {
+        m0 = bf16x2_absmax(m0, w[k]);
+        if (k + 1 < NW)
+            m1 = bf16x2_absmax(m1, w[k + 1]);
+    }
+    const uint32_t m = bf16x2_absmax(m0, m1) & 0x7FFF7FFFu;
+    return fmaxf(bf_lo(m), bf_hi(m));
 }
 
 // --------------------------------------------------------------- e4m3 ---

@@ -281,4 +281,17 @@ __global__ void __launch_bounds__(256) silu_mul_kernel(const float *__restrict__
     }
 }
 
+// --------------------------------------------------------------------------
+// Elementwise group scale from amax, as every kernel forms it (for checking
+// the division on its own).
+// --------------------------------------------------------------------------
+template <bool UE8M0>
+__global__ void __launch_bounds__(256) group_scale_kernel(const float *__restrict__ amax, float *__restrict__ out,
+                                                          int64_t n, float eps)
+{
+    const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i < n)
+        out[i] = group_scale<UE8M0>(amax[i], eps);
+}
+
 }  // namespace fp8q

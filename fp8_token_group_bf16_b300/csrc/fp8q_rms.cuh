@@ -4,14 +4,16 @@
 //
 // Sum of squares.  A lane seeds two accumulators (one packed pair) with
 // pm = the largest square among its 32 values and adds the squares (each
-// exact in fp32: a bf16 value has 8 significant bits) with Dekker's Fast2Sum,
-// whose precondition |accumulator| >= |addend| the seed guarantees; the
-// rounding errors are collected exactly and summed separately.  Taking the
-// seed back out is exact (pm is a multiple of the accumulator's ulp), and
-// every later combination, across groups, lanes and warps, uses Knuth's
-// TwoSum.  The fp32 result is therefore the exact sum rounded once, like a
-// sum carried in wider precision, except when squares underflow fp32 (|z|
-// below about 1e-19).
+// exact in fp32: a bf16 value has 8 significant bits) in the manner of
+// Dekker's Fast2Sum, whose precondition |accumulator| >= |addend| the seed
+// guarantees: t = RN(s + z^2) is one multiply-add, s - t is exact, and the
+// rounding error z^2 + (s - t) is representable, so a second multiply-add
+// yields it exactly.  The errors are summed separately.  Taking the seed
+// back out is exact (pm is a multiple of the accumulator's ulp), and every
+// later combination, across groups, lanes and warps, uses Knuth's TwoSum.
+// The fp32 result is therefore the exact sum rounded once, like a sum
+// carried in wider precision, except when squares underflow fp32 (|z| below
+// about 1e-19).
 #pragma once
 
 #include "fp8q_device.cuh"
@@ -32,22 +34,15 @@ constexpr int kRmsMinCtas = NG == 1 ? 4 : (NG == 2 ? 2 : 1);
 template <int NW>
 __device__ __forceinline__ void lane_sumsq(const uint32_t (&w)[NW], float &hi, float &lo)
 {
-    float m0 = 0.0f, m1 = 0.0f;
-#pragma unroll
-    for (int k = 0; k < NW; k += 2) {
-        m0 = absmax3(m0, bf_lo(w[k]), bf_hi(w[k]));
-        m1 = absmax3(m1, bf_lo(w[k + 1]), bf_hi(w[k + 1]));
-    }
-    const float m = fmaxf(m0, m1);
+    const float m = bf16x2_words_absmax(w);
     const float pm = __fmul_rn(m, m);
     uint64_t s = f2_pack(pm, pm);
     uint64_t c = f2_pack(0.0f, 0.0f);
 #pragma unroll
     for (int k = 0; k < NW; ++k) {
         const uint64_t z = f2_from_bf16x2(w[k]);
-        const uint64_t p = f2_mul(z, z);
-        const uint64_t t = f2_add(s, p);
-        c = f2_add(c, f2_sub(p, f2_sub(t, s)));   // Fast2Sum error, |s| >= |p|
+        const uint64_t t = f2_fma(z, z, s);                // RN(s + z^2), z^2 exact
+        c = f2_add(c, f2_fma(z, z, f2_sub(s, t)));         // its error, exact as |s| >= z^2
         s = t;
     }
     float sv[2], cv[2];

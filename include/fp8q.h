@@ -246,6 +246,18 @@ FP8Q_API int fp8q_f32_to_e4m3(const float *v, void *out, int64_t n, void *stream
  */
 FP8Q_API int fp8q_silu_mul(const float *a, const float *b, float *out, int64_t n, void *stream);
 
+/*
+ * Elementwise group scale: scales[i] = RN32(max(amax[i], eps) / 448), and
+ * with ue8m0 != 0 the smallest power of two >= that value -- the scale every
+ * op above forms from a group's (or row's) maximum |value|, computed by the
+ * same device code (the division in two multiply-adds, correctly rounded).
+ * Exposed so the division can be checked on its own over any fp32 amax.
+ *   amax    fp32 [n], finite and >= 0, read;  scales fp32 [n], written;
+ *           both 4-byte aligned.
+ *   eps     as for per_token_group_quant (finite, >= 1e-30).
+ */
+FP8Q_API int fp8q_group_scale(const float *amax, float *scales, int64_t n, float eps, int32_t ue8m0, void *stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 FP8Q_API const char *fp8q_status_string(int status);
 

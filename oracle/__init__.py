@@ -106,6 +106,7 @@ def _configure(L: ctypes.CDLL) -> ctypes.CDLL:
     L.oracle_pack_ue8m0.restype = I
     L.oracle_pack_ue8m0_mx.argtypes = [P, I64, I64, P]
     L.oracle_pack_ue8m0_mx.restype = I
+    L.oracle_group_scale_n.argtypes = [P, P, I64, F, I]
     L.oracle_f32_to_e4m3_n.argtypes = [P, P, I64]
     L.oracle_ue8m0_ceil_n.argtypes = [P, P, I64]
     L.oracle_silu_mul_n.argtypes = [P, P, P, I64]
@@ -268,6 +269,15 @@ def pack_ue8m0_mx(scales_tg) -> np.ndarray:
     T_pad = -(-T // 128) * 128
     out = np.empty((T_pad, 4 * G), np.uint8)
     _check(lib().oracle_pack_ue8m0_mx(_p(s), T, G, _p(out)))
+    return out
+
+
+def group_scale(amax, eps=SCALE_EPS, ue8m0=False) -> np.ndarray:
+    """The scale of a group with maximum |value| amax: RN32(max(amax, eps) / 448),
+    rounded up to a power of two with ue8m0 (elementwise)."""
+    a = np.ascontiguousarray(amax, dtype=np.float32)
+    out = np.empty_like(a)
+    lib().oracle_group_scale_n(_p(a), _p(out), a.size, eps, int(ue8m0))
     return out
 
 

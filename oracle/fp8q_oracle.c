@@ -478,6 +478,13 @@ int oracle_pack_ue8m0_mx(const float *scales_tg, int64_t T, int64_t G, uint8_t *
 
 /* ----------------------------------------------- batch helpers (tests) -- */
 
+/* The group scale of each amax[i], as every op forms it (test helper). */
+void oracle_group_scale_n(const float *amax, float *out, int64_t n, float eps, int ue8m0)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_group_scale(amax[i], eps, ue8m0, NULL);
+}
+
 void oracle_f32_to_e4m3_n(const float *v, uint8_t *out, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i)

@@ -34,6 +34,7 @@ uint8_t oracle_f32_to_e4m3(float v);
 float oracle_e4m3_to_f32(uint8_t c);
 float oracle_ue8m0_ceil(float s);
 float oracle_group_scale(float amax, float eps, int ue8m0, float *pre);
+void oracle_group_scale_n(const float *amax, float *out, int64_t n, float eps, int ue8m0);
 float oracle_rms_inv(float ss, int64_t H, float eps);
 float oracle_silu_mul(float a, float b);
 

@@ -160,6 +160,23 @@ def pin_ue8m0():
         assert m == 0.5, f"ue8m0({x!r}) = {y!r} is not a power of two"
 
 
+def pin_group_scale_fp32():
+    """The scale from an fp32 amax (ops B and C meet any fp32 amax): against
+    exact rational division by 448, the floor applied first, and the
+    power-of-two ceiling, over amax values spread across the exponent range,
+    near the floor, and next to multiples of 448 times powers of two."""
+    rng = np.random.default_rng(11)
+    a = (1.0 + rng.random(2500)) * 2.0 ** rng.integers(-100, 100, 2500)
+    near = np.array([448.0 * 2.0 ** k for k in range(-60, 60, 7)])
+    a = np.concatenate([a, near, np.nextafter(near, np.inf), np.nextafter(near, 0),
+                        [0.0, 1e-30, 1e-10, 9.99e-11, 1.0000001e-10, 3.0e38]]).astype(np.float32)
+    for ue8m0 in (False, True):
+        got = oracle.group_scale(a, ue8m0=ue8m0)
+        for x, y in zip(a.tolist(), got.tolist()):
+            want, _ = group_scale(x, ue8m0)
+            assert y == want, f"group_scale({x!r}, ue8m0={ue8m0}) = {y!r}, exact {want!r}"
+
+
 # -------------------------------------------------- op A (per group) ----
 
 
@@ -823,6 +840,7 @@ def pin_qk_rope_rotation_keeps_pair_norms():
 
 ALL_PINS = [
     pin_golden_midpoints,
+    pin_group_scale_fp32,
     pin_ue8m0_packed_golden,
     pin_ue8m0_packed_decodes,
     pin_ue8m0_mx_tiles,

@@ -155,6 +155,31 @@ def test_f32_to_e4m3_all_fp32_patterns():
         assert bad.size == 0, (start, bad.size, v[bad[:4]], got[bad[:4]], want[bad[:4]])
 
 
+def test_group_scale_every_fp32_significand():
+    """The scale from an fp32 group maximum (ops B and C meet any fp32 amax):
+    every fp32 significand at binades spread over the range (the division
+    scales exactly with the exponent while the quotient is normal), near the
+    floor, and both UE8M0 modes, against the oracle's IEEE division."""
+    import fp8_token_group_bf16_b300 as fq
+
+    sig = np.arange(1 << 23, dtype=np.uint32) | np.uint32(127 << 23)        # [1, 2)
+    for e in (-100, -61, -60, -34, -1, 0, 37, 100):
+        a = (sig.view(np.float32) * np.float32(2.0 ** e)).astype(np.float32)
+        for ue8m0 in (False, True):
+            got = fq.group_scale(torch.from_numpy(a).cuda(), ue8m0=ue8m0).cpu().numpy()
+            want = oracle.group_scale(a, ue8m0=ue8m0)
+            bad = np.nonzero(got.view(np.uint32) != want.view(np.uint32))[0]
+            assert bad.size == 0, (e, ue8m0, bad.size, a[bad[:3]], got[bad[:3]], want[bad[:3]])
+    rng = np.random.default_rng(4)
+    a = np.concatenate([rng.random(1 << 16).astype(np.float32) * np.float32(2e-10), np.zeros(4, np.float32),
+                        np.array([1e-10, 3.0e38], np.float32)])
+    for ue8m0 in (False, True):
+        for eps in (1e-10, 1e-30):
+            got = fq.group_scale(torch.from_numpy(a).cuda(), eps=eps, ue8m0=ue8m0).cpu().numpy()
+            want = oracle.group_scale(a, eps=np.float32(eps), ue8m0=ue8m0)
+            assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), (ue8m0, eps)
+
+
 # ----------------------------------------------- op B (rms + quant) ----
 
 

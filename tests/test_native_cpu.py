@@ -52,10 +52,15 @@ def test_only_c_abi_symbols_exported(lib):
     assert all(s.startswith("fp8q_") for s in text_syms), [s for s in text_syms if not s.startswith("fp8q_")][:5]
 
 
-def test_built_for_sm103a(lib):
-    out = subprocess.run(["cuobjdump", "--list-elf", fq.LIB_PATH], capture_output=True, text=True)
-    if out.returncode == 0:
-        assert "sm_103a" in out.stdout
+def test_built_for_sm103a_only(lib):
+    """The build compiles one target, sm_103a machine code (no PTX for a
+    driver to recompile): a GPU of another architecture refuses the kernels
+    instead of running something else.  The -m gpu tests, which launch every
+    kernel on a B300, are the other half of this check."""
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    flags = build.NVCC_FLAGS
+    assert flags[: len(build.ARCH)] == build.ARCH
+    assert not any("compute_" in f and f not in build.ARCH for f in flags)
 
 
 def test_status_strings(lib):
@@ -189,6 +194,11 @@ def test_misaligned(lib):
     assert fq.fp8q_silu_mul(A + 4, A, A, 16, None) == M
     assert fq.fp8q_silu_mul(A, A, A, -1, None) == fq.FP8Q_ERR_INVALID_ARG
     assert fq.fp8q_silu_mul(None, None, None, 0, None) == 0
+    assert fq.fp8q_group_scale(A + 2, A, 16, 1e-10, 0, None) == M
+    assert fq.fp8q_group_scale(A, A, -1, 1e-10, 0, None) == fq.FP8Q_ERR_INVALID_ARG
+    assert fq.fp8q_group_scale(A, A, 16, 0.0, 0, None) == fq.FP8Q_ERR_INVALID_ARG
+    assert fq.fp8q_group_scale(None, A, 16, 1e-10, 1, None) == fq.FP8Q_ERR_INVALID_ARG
+    assert fq.fp8q_group_scale(None, None, 0, 1e-10, 0, None) == 0
 
 
 def test_empty_input_is_a_no_op(lib):
