@@ -3,6 +3,7 @@
 #include "fp8q.h"
 #include "fp8q_kernels.cuh"
 #include "fp8q_rms.cuh"
+#include "fp8q_rms_split.cuh"
 #include "fp8q_rope.cuh"
 #include "fp8q_token.cuh"
 
@@ -172,11 +173,39 @@ cudaError_t launch_rms_row(const uint16_t *x, uint16_t *res, const uint16_t *w, 
     return launch(rms_row_kernel<NG, U, C, R, V, false>, grid, block, st, x, res, w, q, s, T, H, G, eps, 0);
 }
 
+// rms_norm_per_block_quant for at most kRmsSplitMaxRows rows of more than 64
+// groups: each row over a cluster of up to 8 CTAs (rms_split_kernel) of
+// gpc = max(16, ceil(G / 8)) groups.  Measured at T = 1 / 8 / 32 against the
+// CTA per row: H = 32768 2.08 / 2.25 / 3.01 us against 3.67 / 3.73 / 4.00;
+// H = 16384 2.01 / 2.16 / 2.63 against 2.26 / 2.27 / 2.72; H = 12288 1.98 /
+// 2.11 / 2.18 against 2.12 / 2.15 / 2.23; equal at T = 64.  For rows of up to
+// 64 groups the split lost at every T from 1 to 512 (H = 5120, T = 1: 1.78
+// against 1.58 us): its two cluster barriers cost more than the shorter
+// per-SM chains save.
+constexpr int kRmsSplitMaxRows = 64;
+
+template <bool U, int C, bool R, bool V>
+cudaError_t launch_rms_split(const uint16_t *x, uint16_t *res, const uint16_t *w, uint8_t *q, float *s, int T,
+                             int H, int G, float eps, cudaStream_t st)
+{
+    int gpc = std::max(16, (G + 7) / 8);
+    const int cl = (G + gpc - 1) / gpc;   // 2..8 for 64 < G <= 256
+    gpc = (G + cl - 1) / cl;              // balanced: no CTA is left without groups
+    const int threads = ((gpc * 4 + 31) / 32) * 32;
+    return launch_ex(rms_split_kernel<U, C, R, V>, dim3{unsigned(T * cl)}, dim3{unsigned(threads)}, unsigned(cl), 0,
+                     st, x, res, w, q, s, T, H, G, gpc, cl, eps);
+}
+
 template <bool U, int C, bool R>
 cudaError_t launch_rms(const uint16_t *x, uint16_t *res, const uint16_t *w, uint8_t *q, float *s,
                        int T, int H, int G, float eps, cudaStream_t st)
 {
     const bool v8 = aligned(x, 32) && aligned(q, 32) && aligned(w, 32) && (!res || aligned(res, 32));
+    if constexpr (C != kPerToken) {
+        if (G > 64 && T <= kRmsSplitMaxRows)
+            return v8 ? launch_rms_split<U, C, R, true>(x, res, w, q, s, T, H, G, eps, st)
+                      : launch_rms_split<U, C, R, false>(x, res, w, q, s, T, H, G, eps, st);
+    }
 #define FP8Q_ROW(NG)                                                                             \
     (v8 ? launch_rms_row<NG, U, C, R, true>(x, res, w, q, s, T, H, G, eps, st)                  \
         : launch_rms_row<NG, U, C, R, false>(x, res, w, q, s, T, H, G, eps, st))

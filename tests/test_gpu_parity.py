@@ -330,9 +330,12 @@ def test_rms_bit_exact_shapes(T, H):
 
 @pytest.mark.parametrize("T,H,residual", [(1100, 4096, True), (1024, 5120, False), (2048, 8192, True),
                                           (1500, 384, True), (1031, 1152, False), (64, 16384, True),
-                                          (33, 12288, False), (9, 32768, True), (17, 20480, False)])
+                                          (33, 12288, False), (9, 32768, True), (17, 20480, False),
+                                          (400, 12288, False), (200, 20480, False), (160, 32768, False)])
 def test_rms_many_rows_bit_exact(T, H, residual):
-    """Larger launches, ragged group counts, and rows of 1, 2 and 4 groups per quad."""
+    """Larger launches, ragged group counts, rows of 1, 2 and 4 groups per quad,
+    and (T > 64 without the residual) their builds that prefetch a later row
+    into L2 once the grid outlasts the CTAs resident at once."""
     x, w, r = inputs.rms_input(T, H, seeds=(910 + T, 911 + H, 912))
     xb, wb, rb = inputs.bits(x), inputs.bits(w), inputs.bits(r) if residual else None
     for ue8m0, col in VARIANTS:
