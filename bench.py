@@ -145,6 +145,9 @@ class Dist:
     def sum(self, v: float) -> float:
         return self._reduce(v, "sum")
 
+    def min(self, v: float) -> float:
+        return -self._reduce(-v, "max")
+
     def _reduce(self, v: float, op: str) -> float:
         if self.pg is None:
             return float(v)
@@ -410,10 +413,10 @@ class DeviceStep:
 
 def time_device(step: DeviceStep, steps: int, warmup: int, dist: Dist):
     """K steps of the three launches back to back, bracketed by barrier +
-    synchronize, timed with one pair of CUDA events on the launching stream
-    (an event between two kernels would stop the second from being
-    scheduled while the first drains).  Then K more steps with an event
-    after every launch give each kernel's average duration."""
+    synchronize, timed with one pair of CUDA events on the launching stream.
+    No event sits between two kernels: it would stop the second from being
+    scheduled while the first drains (the per-op figures come from
+    per_op_records and chain_record instead)."""
     import torch
 
     st = step.stream
@@ -433,20 +436,7 @@ def time_device(step: DeviceStep, steps: int, warmup: int, dist: Dist):
     torch.cuda.synchronize()
     t1 = time.perf_counter()
     dist.barrier()
-    total_ms = start.elapsed_time(end)
-
-    per_op = {op: [] for op in step.ops}
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(step.ops) + 1)] for _ in range(steps)]
-    for k in range(steps):
-        ev[k][0].record(st)
-        for i, op in enumerate(step.ops):
-            step.launch(op)
-            ev[k][i + 1].record(st)
-    torch.cuda.synchronize()
-    for k in range(steps):
-        for i, op in enumerate(step.ops):
-            per_op[op].append(ev[k][i].elapsed_time(ev[k][i + 1]))
-    return total_ms / 1e3, {op: sum(v) / len(v) for op, v in per_op.items()}, (t0, t1)
+    return start.elapsed_time(end) / 1e3, (t0, t1)
 
 
 class E2EPipeline:
@@ -584,7 +574,10 @@ def time_e2e(host, steps: int, dist: Dist, chunks: int = 8):
     dist.barrier()
     agg = aggregate(step_bytes(pipe.T) * steps, secs, dist, steps)
     link = host_link_ceiling(pipe.h2d, pipe.d2h)
+    # the slowest rank's link against the slowest rank's step time
+    link = {k: round(dist.min(v), 1) for k, v in link.items()}
     link["frac"] = round((pipe.h2d + pipe.d2h) / (agg["ms_per_step"] * 1e-3) / 1e9 / link["both_GBps"], 4)
+    link["ranks"] = "each rate is the minimum over ranks"
     return {"value": round(agg["value"], 2), "unit": UNIT, "h2d_bytes_per_step": pipe.h2d,
             "d2h_bytes_per_step": pipe.d2h, "steps": steps, "ms_per_step": round(agg["ms_per_step"], 3),
             "pipeline": f"{len(pipe.bounds)} token slices, copy-in / compute / copy-out streams",
@@ -667,6 +660,152 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------ isolated op timing --
+
+L2_BYTES = 126 << 20
+RECORD_T = (512, 4096, 16384)   # the per-op record of the default run
+CHAIN_T = 512
+STEP_SHAPES = {   # op: (row length H or I, scale layout) as in the step
+    "per_token_group_fp8_quant": (A_H, "col"),
+    "rms_norm_per_block_quant": (B_H, "row"),
+    "silu_and_mul_per_block_quant": (C_I, "row"),
+}
+
+
+def graph_time_us(make, nbytes: int, iters: int, reps: int = 5) -> float:
+    """Per-launch device time (us) of `iters` back-to-back calls captured in
+    one CUDA graph, cycling over enough independent buffer sets (each from
+    make()) that their bytes exceed 3x L2, so no call finds its inputs in L2
+    from an earlier one.  Median over `reps` replays, each bracketed by CUDA
+    events on the stream the graph is replayed on."""
+    import torch
+
+    nsets = min(64, max(2, int(3 * L2_BYTES // max(nbytes, 1)) + 1))
+    calls = [make() for _ in range(nsets)]
+    for c in calls:
+        c()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g):
+            for k in range(iters):
+                calls[k % nsets]()
+    g.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) / iters)
+    del g, calls
+    torch.cuda.empty_cache()
+    return statistics.median(ts) * 1e3
+
+
+def copy_maker(nbytes: int):
+    """A same-size copy on the SMs (an elementwise x * 1 over fp32 words,
+    reading and writing nbytes in total): a plain device-to-device memcpy may
+    be handed to a copy engine, which is slower at some sizes."""
+    import torch
+
+    def make():
+        n = max(1, nbytes // 8)
+        a = torch.zeros(n, dtype=torch.float32, device="cuda")
+        b = torch.empty(n, dtype=torch.float32, device="cuda")
+        return lambda: torch.mul(a, 1.0, out=b)
+    return make
+
+
+def step_op_maker(op: str, T: int, seed: int):
+    """make() for one of the step's ops at T tokens, with the step's options
+    (UE8M0; op A column-major scales) on fresh device buffers drawn from the
+    step's distributions by a seeded device generator."""
+    import torch
+
+    import fp8_token_group_bf16_b300 as fq
+    from fp8_token_group_bf16_b300 import inputs
+
+    H, lay = STEP_SHAPES[op]
+    G = H // GROUP
+    counter = [0]
+
+    def make():
+        counter[0] += 1
+        sd = seed + 7919 * counter[0]
+        q = torch.empty(T, H, dtype=torch.float8_e4m3fn, device="cuda")
+        if op == "per_token_group_fp8_quant":
+            x = inputs.device_heavy_tailed_input(T, H, sd, "cuda")
+            s = torch.empty(G, T, device="cuda").t()
+            return lambda: fq.per_token_group_fp8_quant(x, ue8m0=True, column_major_scales=True, q=q, scales=s)
+        s = torch.empty(T, G, device="cuda")
+        if op == "rms_norm_per_block_quant":
+            x = inputs.device_lognormal_channel_input(T, H, sd, "cuda")
+            w = (1.0 + 0.1 * torch.randn(H, generator=torch.Generator(device="cuda").manual_seed(sd + 1),
+                                         device="cuda")).to(torch.bfloat16)
+            return lambda: fq.rms_norm_per_block_quant(x, w, None, ue8m0=True, q=q, scales=s)
+        x = inputs.device_lognormal_channel_input(T, 2 * H, sd, "cuda")
+        return lambda: fq.silu_and_mul_per_block_quant(x, ue8m0=True, q=q, scales=s)
+    return make
+
+
+def _iters(nbytes: int) -> int:
+    return 200 if nbytes < 50e6 else 40
+
+
+def per_op_records(peak: float, T_values=RECORD_T) -> list:
+    """The metric itself: each of the step's three ops alone at each T, its
+    algorithmic bytes over its per-launch time (graph replay, inputs rotated
+    past L2), beside a same-size SM copy timed the same way."""
+    rows = []
+    for T in T_values:
+        for i, op in enumerate(STEP_SHAPES):
+            H, lay = STEP_SHAPES[op]
+            nbytes = algorithmic_bytes(op, T, H)
+            us = graph_time_us(step_op_maker(op, T, 9000 + 10 * T + i), nbytes, _iters(nbytes))
+            cus = graph_time_us(copy_maker(nbytes), nbytes, _iters(nbytes))
+            gbs, cgbs = nbytes / us / 1e3, nbytes / cus / 1e3
+            rows.append({"op": op, "T": T, "H_or_I": H, "scales": f"UE8M0 {lay}-major", "bytes": nbytes,
+                         "us": round(us, 3), "GBps": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                         "copy_us": round(cus, 3), "copy_GBps": round(cgbs, 1),
+                         "copy_frac_of_peak": round(cgbs / peak, 4)})
+    return rows
+
+
+def chain_record(peak: float, T: int = CHAIN_T) -> dict:
+    """The step's three ops back to back at T as dependent launches (no event
+    between them), in one graph over rotated buffer sets; ops A and B get
+    their marginal cost inside the chain: t(A, B, C) - t(B, C) and
+    t(A, B, C) - t(A, C)."""
+    ops = list(STEP_SHAPES)
+    makers = {op: step_op_maker(op, T, 9500 + i) for i, op in enumerate(ops)}
+    nb = {op: algorithmic_bytes(op, T, STEP_SHAPES[op][0]) for op in ops}
+
+    def chain(sel):
+        def make():
+            calls = [makers[op]() for op in sel]
+
+            def run():
+                for c in calls:
+                    c()
+            return run
+        nbytes = sum(nb[op] for op in sel)
+        return graph_time_us(make, nbytes, _iters(nbytes))
+
+    t_abc, t_bc, t_ac = chain(ops), chain(ops[1:]), chain([ops[0], ops[2]])
+    out = {"T": T, "step_us": round(t_abc, 3), "step_GBps": round(sum(nb.values()) / t_abc / 1e3, 1),
+           "method": "graph of back-to-back dependent launches (A, B, C), buffers rotated past 3x L2; "
+                     "marginal = t(A,B,C) minus the chain without the op"}
+    for op, rest in ((ops[0], t_bc), (ops[1], t_ac)):
+        m = t_abc - rest
+        out[op] = {"marginal_us": round(m, 3), "GBps": round(nb[op] / m / 1e3, 1) if m > 0 else None,
+                   "frac_of_peak": round(nb[op] / m / 1e3 / peak, 4) if m > 0 else None}
+    return out
+
+
 # ------------------------------------------------------------------ sweep --
 
 
@@ -681,42 +820,7 @@ def sweep(args):
     fq.load()
     dev = torch.device("cuda")
     peak, peak_kind = load_peaks()
-    l2 = 126 << 20
-
-    def timed(make, nbytes, iters):
-        nsets = min(64, max(2, int(3 * l2 // max(nbytes, 1)) + 1))
-        calls = [make() for _ in range(nsets)]
-        for c in calls:
-            c()
-        torch.cuda.synchronize()
-        s = torch.cuda.Stream()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(s):
-            with torch.cuda.graph(g):
-                for k in range(iters):
-                    calls[k % nsets]()
-        g.replay()
-        torch.cuda.synchronize()
-        ts = []
-        for _ in range(5):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            g.replay()
-            b.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b) / iters)
-        del g, calls
-        return statistics.median(ts) * 1e3
-
-    def copy_maker(nbytes):
-        # an SM-side copy (elementwise x * 1 on fp32 words): a plain D2D memcpy
-        # may be handed to a copy engine, which is slower at some sizes
-        def make():
-            n = max(1, nbytes // 8)
-            a = torch.zeros(n, dtype=torch.float32, device=dev)
-            b = torch.empty(n, dtype=torch.float32, device=dev)
-            return lambda: torch.mul(a, 1.0, out=b)
-        return make
+    timed = graph_time_us
 
     e4 = torch.float8_e4m3fn
     points = []   # (op, T, H or I, ue8m0, scale layout, residual)
@@ -902,6 +1006,8 @@ def parse_args(argv=None):
     p.add_argument("--packed", action="store_true", help="with --op: packed UE8M0 scales (per-group ops)")
     p.add_argument("--mx", action="store_true", help="with --op: MXFP8 scale tiles (per-group ops)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-records", action="store_true",
+                   help="skip the per-op T records and the chained step (for profiling the step alone)")
     p.add_argument("--tokens", type=int, default=STEP_T,
                    help="tokens per step (default: the T=4096 workload; smaller values are for profiling)")
     p.add_argument("--reference-budget-s", type=float, default=120.0,
@@ -939,37 +1045,58 @@ def main(argv=None):
         host = workload_inputs(T)
         stream = torch.cuda.Stream()
         step = DeviceStep(host, stream, T)
+        peak, peak_kind = load_peaks()
         clocks = ClockSampler(torch.cuda.current_device()).start()
         try:
-            secs, per_op_ms, window = time_device(step, args.steps, args.warmup, dist)
+            secs, window = time_device(step, args.steps, args.warmup, dist)
+            records, chain = None, None
+            if not args.no_records:
+                # isolated per-op records and the chained step, rank 0 only (one GPU's figures)
+                records = per_op_records(peak) if dist.rank == 0 else None
+                chain = chain_record(peak) if dist.rank == 0 else None
+            t_end = time.perf_counter()
         finally:
             clocks.stop()
         agg = aggregate(step_bytes(T) * args.steps, secs, dist, args.steps)
-        peak, peak_kind = load_peaks()
-        dom_ms = per_op_ms[DOMINANT]
-        achieved = step.bytes[DOMINANT] / (dom_ms * 1e-3) / 1e9
+        # the dominant kernel alone at the step's T, from its isolated record
+        # (graph replay on the launching stream, CUDA events around the replay)
+        dom = next((r for r in records or [] if r["op"] == DOMINANT and r["T"] == T), None)
+        roofline = {"bound": "hbm", "kernel": KERNEL_NAMES[DOMINANT], "unit": "GB/s", "peak": peak,
+                    "peak_source": (f"{peak_kind}: MEASURED_PEAKS.json hbm_gbs (device copy bandwidth, burst: "
+                                    "the kernel is timed alone)" if peak_kind == "measured"
+                                    else "fallback 6.4 TB/s")}
         traffic = recorded_traffic(KERNEL_NAMES[DOMINANT], f"T={T} I={C_I} ue8m0 row")
+        if dom is not None:
+            roofline.update({"achieved": dom["GBps"], "frac": dom["frac_of_peak"],
+                             "algorithmic_bytes_per_launch": dom["bytes"], "us_per_launch": dom["us"],
+                             "timing": "isolated launches in a CUDA graph over buffers rotated past 3x L2",
+                             "nominal_peak": NOMINAL_HBM_GBS,
+                             "frac_of_nominal": round(dom["GBps"] / NOMINAL_HBM_GBS, 4)})
+        roofline["traffic"] = traffic
+        roofline["traffic_source"] = ("recorded, not measured in this run: DRAM read + write bytes per launch "
+                                      "from the committed ncu summary profiles/dram_traffic.txt, taken on the "
+                                      "current kernel sources (hash-checked)" if traffic is not None else
+                                      "null: no ncu summary of the current kernel sources")
         e2e = time_e2e(host, args.e2e_steps, dist)
         line = {
             "metric": METRIC, "value": round(agg["value"], 2), "unit": UNIT, "n_gpus": dist.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(agg["ms_per_step"], 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded generators; no dataset)", "config": step_config(T),
-            "roofline": {"bound": "hbm", "kernel": KERNEL_NAMES[DOMINANT], "achieved": round(achieved, 1),
-                         "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "peak_source": (f"{peak_kind}: MEASURED_PEAKS.json hbm_gbs (device copy bandwidth)"
-                                         if peak_kind == "measured" else "fallback 6.4 TB/s"),
-                         "traffic": traffic,
-                         "algorithmic_bytes_per_launch": step.bytes[DOMINANT],
-                         "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4)},
-            "ops": {op: {"us_per_launch": round(ms * 1e3, 2),
-                         "GBps": round(step.bytes[op] / (ms * 1e-3) / 1e9, 1),
-                         "frac_of_peak": round(step.bytes[op] / (ms * 1e-3) / 1e9 / peak, 4),
-                         "bytes": step.bytes[op]} for op, ms in per_op_ms.items()},
+            "roofline": roofline,
             "e2e": e2e,
             "gpu_launches": len(step.ops) * args.steps,
-            "clocks": clocks.summary(*window),
+            "clocks": dict(clocks.summary(window[0], t_end),
+                           window_covers="the timed steps, then the per-op records and the chained step"),
         }
+        if records is not None:
+            line["per_op"] = records
+            line["per_op_method"] = ("each op alone at T, graph replay of back-to-back launches over buffer "
+                                     "sets rotated past 3x L2, median of 5 replays; copy = a same-size SM copy "
+                                     "timed the same way; inputs drawn on the device from the step's "
+                                     "distributions")
+        if chain is not None:
+            line["chain_T512"] = chain
         if dist.rank == 0 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(host, T)
         if dist.rank == 0:

@@ -234,6 +234,32 @@ def mix_seed(T: int) -> int:
 
 
 # --------------------------------------------------------------------------
+# The same two recipes drawn on a CUDA device (for timing at sizes where
+# drawing on the host would take longer than the measurement): a seeded
+# device generator, the same distributions, bf16 on the device.  The values
+# differ from the host draws of the same seed.
+# --------------------------------------------------------------------------
+
+
+def device_heavy_tailed_input(T: int, H: int, seed: int, device) -> torch.Tensor:
+    g = torch.Generator(device=device).manual_seed(seed)
+    x = torch.randn(T * H, generator=g, device=device)
+    n_out = int(round(0.001 * T * H))
+    if n_out:
+        pos = torch.randperm(T * H, generator=g, device=device)[:n_out]
+        x[pos] *= 100.0
+    return x.view(T, H).to(torch.bfloat16)
+
+
+def device_lognormal_channel_input(T: int, C: int, seed: int, device) -> torch.Tensor:
+    g = torch.Generator(device=device).manual_seed(seed)
+    sigma = torch.exp(torch.randn(C, generator=g, device=device))
+    x = torch.randn(T, C, generator=g, device=device)
+    x.mul_(sigma)
+    return x.to(torch.bfloat16)
+
+
+# --------------------------------------------------------------------------
 # fused_qk_norm_rope case, Qwen3-32B attention shape: 64 query heads and 8
 # key/value heads of 128 values per token; query/key activations with
 # per-channel spread (lognormal channel std), value heads N(0,1); norm

@@ -58,7 +58,10 @@ def _rank_main(rank, world, port, out):
     try:
         d.barrier()
         # rank r processed (r+1) GB in (r+1) * 0.5 s
-        out[rank] = bench.aggregate(1e9 * (rank + 1), 0.5 * (rank + 1), d, steps=10)
+        agg = bench.aggregate(1e9 * (rank + 1), 0.5 * (rank + 1), d, steps=10)
+        # the host-link rate of the e2e record is the slowest rank's
+        agg["min_link"] = d.min(10.0 * (rank + 1))
+        out[rank] = agg
     finally:
         d.close()
 
@@ -81,6 +84,7 @@ def test_weak_scaling_aggregate_two_gloo_ranks():
         assert agg["total_bytes"] == 3e9          # every rank's bytes
         assert abs(agg["value"] - 3.0) < 1e-12    # GB/s of the whole job
         assert abs(agg["ms_per_step"] - 100.0) < 1e-9
+        assert agg["min_link"] == 10.0            # min over ranks
 
 
 def test_single_process_aggregate():
