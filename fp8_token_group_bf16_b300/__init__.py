@@ -211,11 +211,29 @@ def _layout(column_major_scales, packed_ue8m0_scales, ue8m0, mx_scales=False):
     return FP8Q_SCALES_COL_MAJOR if column_major_scales else FP8Q_SCALES_ROW_MAJOR
 
 
+def _same_device(name, t, x):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or t.device != x.device:
+        raise ValueError(f"{name} must be a tensor on {x.device}, the device of x")
+
+
+def _check_q(q, x, T, cols):
+    """A caller's code buffer: one byte per value, [T, cols], contiguous, on x's device."""
+    _same_device("q", q, x)
+    if tuple(q.shape) != (T, cols) or q.element_size() != 1 or not q.is_contiguous():
+        raise ValueError(f"q must be a contiguous 1-byte tensor of shape [{T}, {cols}]")
+    return q
+
+
 def _outputs(x, T, cols, group_size, layout, q, scales):
     torch = _torch()
     G = cols // group_size
     if q is None:
         q = torch.empty((T, cols), dtype=torch.float8_e4m3fn, device=x.device)
+    else:
+        _check_q(q, x, T, cols)
+    if scales is not None:
+        _same_device("scales", scales, x)
     if scales is None:
         if layout == FP8Q_SCALES_UE8M0_PACKED:
             scales = torch.empty(packed_scale_shape(T, G), dtype=torch.int32, device=x.device)
@@ -240,7 +258,8 @@ def _scale_ptr(scales, T, G, layout):
             raise ValueError(f"packed scales must be a contiguous int32 tensor of shape {packed_scale_shape(T, G)}")
         return scales.data_ptr()
     want = (1, T) if layout == FP8Q_SCALES_COL_MAJOR else (G, 1)
-    if tuple(scales.shape) != (T, G) or (T > 1 and G > 1 and tuple(scales.stride()) != want):
+    if scales.dtype != _torch().float32 or tuple(scales.shape) != (T, G) or \
+            (T > 1 and G > 1 and tuple(scales.stride()) != want):
         raise ValueError(f"scales must be a [T, G] = [{T}, {G}] fp32 tensor with strides {want}")
     return scales.data_ptr()
 
@@ -277,8 +296,10 @@ def rms_norm_per_block_quant(x, weight, residual=None, eps: float = 1e-6, group_
     the value that is normalised.  Returns (q, scales)."""
     _need_cuda_bf16("x", x)
     _need_cuda_bf16("weight", weight)
+    _same_device("weight", weight, x)
     if residual is not None:
         _need_cuda_bf16("residual", residual)
+        _same_device("residual", residual, x)
         if residual.shape != x.shape:
             raise ValueError("residual must have the shape of x")
     if x.dim() != 2 or weight.dim() != 1 or weight.shape[0] != x.shape[1]:
@@ -318,8 +339,11 @@ def _token_outputs(x, T, cols, q, scales):
     torch = _torch()
     if q is None:
         q = torch.empty((T, cols), dtype=torch.float8_e4m3fn, device=x.device)
+    else:
+        _check_q(q, x, T, cols)
     if scales is None:
         scales = torch.empty((T, 1), dtype=torch.float32, device=x.device)
+    _same_device("scales", scales, x)
     if scales.numel() != T or scales.dtype != torch.float32 or not scales.is_contiguous():
         raise ValueError(f"per-token scales must be a contiguous fp32 tensor of {T} elements")
     return q, scales
@@ -347,8 +371,10 @@ def rms_norm_dynamic_per_token_quant(x, weight, residual=None, eps: float = 1e-6
     rms_norm_per_block_quant.  Returns (q [T, H], scales [T, 1])."""
     _need_cuda_bf16("x", x)
     _need_cuda_bf16("weight", weight)
+    _same_device("weight", weight, x)
     if residual is not None:
         _need_cuda_bf16("residual", residual)
+        _same_device("residual", residual, x)
         if residual.shape != x.shape:
             raise ValueError("residual must have the shape of x")
     if x.dim() != 2 or weight.dim() != 1 or weight.shape[0] != x.shape[1]:
@@ -387,6 +413,7 @@ def fused_qk_norm_rope(qkv, q_weight, k_weight, cos_sin, positions, num_q_heads:
     torch = _torch()
     for name, t in (("qkv", qkv), ("q_weight", q_weight), ("k_weight", k_weight), ("cos_sin", cos_sin)):
         _need_cuda_bf16(name, t)
+        _same_device(name, t, qkv)
     if positions.device != qkv.device or positions.dtype != torch.int64 or not positions.is_contiguous():
         raise ValueError("positions must be a contiguous int64 tensor on the device of qkv")
     T = qkv.shape[0]
@@ -407,10 +434,12 @@ def silu_mul(a, b, out=None, stream=None):
     for name, t in (("a", a), ("b", b)):
         if t.device.type != "cuda" or t.dtype != torch.float32 or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous fp32 CUDA tensor")
-    if a.shape != b.shape:
-        raise ValueError("a and b must have the same shape")
+    if a.shape != b.shape or a.device != b.device:
+        raise ValueError("a and b must have the same shape and device")
     if out is None:
         out = torch.empty_like(a)
+    elif out.device != a.device or out.dtype != torch.float32 or out.shape != a.shape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous fp32 tensor shaped like a, on a's device")
     _check(fp8q_silu_mul(a.data_ptr(), b.data_ptr(), out.data_ptr(), a.numel(), _stream_ptr(a, stream)), "silu_mul")
     return out
 
@@ -422,6 +451,9 @@ def group_scale(amax, eps: float = 1e-10, ue8m0: bool = False, out=None, stream=
         raise ValueError("amax must be a contiguous fp32 CUDA tensor")
     if out is None:
         out = torch.empty_like(amax)
+    elif out.device != amax.device or out.dtype != torch.float32 or out.shape != amax.shape or \
+            not out.is_contiguous():
+        raise ValueError("out must be a contiguous fp32 tensor shaped like amax, on its device")
     _check(fp8q_group_scale(amax.data_ptr(), out.data_ptr(), amax.numel(), eps, int(ue8m0), _stream_ptr(amax, stream)),
            "group_scale")
     return out
@@ -434,6 +466,8 @@ def f32_to_e4m3(v, out=None, stream=None):
         raise ValueError("v must be a contiguous fp32 CUDA tensor")
     if out is None:
         out = torch.empty(v.shape, dtype=torch.uint8, device=v.device)
+    elif out.device != v.device or out.element_size() != 1 or out.numel() != v.numel() or not out.is_contiguous():
+        raise ValueError("out must be a contiguous 1-byte tensor with v's element count, on v's device")
     _check(fp8q_f32_to_e4m3(v.data_ptr(), out.data_ptr(), v.numel(), _stream_ptr(v, stream)),
            "f32_to_e4m3")
     return out

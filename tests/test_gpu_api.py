@@ -181,11 +181,11 @@ def test_packed_scales_no_writes_outside(T, H, op, mx):
     assert not bool((s.view(torch.uint8) == 0xA5).any()), "every packed byte is written"
 
 
-@pytest.mark.parametrize("T,H", [(1, 128), (3, 896), (7, 8320), (2, 65536)])
-@pytest.mark.parametrize("op", ["token", "token_silu", "token_rms"])
-def test_per_token_no_writes_outside(T, H, op):
-    if op == "token_rms" and H > fq.FP8Q_RMS_MAX_H:
-        pytest.skip("longer than the RMSNorm row limit")
+# (the RMSNorm variant's rows end at FP8Q_RMS_MAX_H = 32768; longer rows are rejected, see test_native_cpu)
+@pytest.mark.parametrize("op,T,H", [(op, T, H) for op in ("token", "token_silu", "token_rms")
+                                    for T, H in ((1, 128), (3, 896), (7, 8320), (2, 65536), (2, 32768))
+                                    if not (op == "token_rms" and H > fq.FP8Q_RMS_MAX_H)])
+def test_per_token_no_writes_outside(op, T, H):
     xb = inputs.bits(inputs.heavy_tailed_input(T, 2 * H if op == "token_silu" else H, seed=T + 11 * H))
     x = dev_bf16(xb)
     qraw, q = _guarded(T * H)
@@ -269,3 +269,53 @@ def test_tensor_api_rejects_wrong_scale_buffers():
                                         scales=torch.empty(fq.mx_scale_shape(5, G), dtype=torch.uint8, device="cuda"))
     torch.cuda.synchronize()
     assert s.shape == (128, 4 * G)
+
+
+def test_tensor_api_checks_caller_buffers():
+    """Output buffers passed in by the caller are checked before their raw
+    pointers reach the kernels: shape, element size, contiguity, dtype of
+    fp32 scales, and the device of every tensor."""
+    x = torch.zeros(8, 512, dtype=torch.bfloat16, device="cuda")
+    w = torch.ones(512, dtype=torch.bfloat16, device="cuda")
+    e4 = torch.float8_e4m3fn
+    bad_q = [torch.empty(4, 512, dtype=e4, device="cuda"),                   # too few rows
+             torch.empty(8, 1024, dtype=e4, device="cuda")[:, ::2],          # strided
+             torch.empty(8, 512, dtype=torch.bfloat16, device="cuda"),       # 2-byte elements
+             torch.empty(8, 512, dtype=e4)]                                  # on the host
+    for q in bad_q:
+        with pytest.raises(ValueError, match="q must be"):
+            fq.per_token_group_fp8_quant(x, q=q)
+        with pytest.raises(ValueError, match="q must be"):
+            fq.rms_norm_per_block_quant(x, w, q=q)
+        with pytest.raises(ValueError, match="q must be"):
+            fq.dynamic_per_token_scaled_fp8_quant(x, q=q)
+    with pytest.raises(ValueError, match="q must be"):
+        fq.silu_and_mul_per_block_quant(x, q=torch.empty(8, 512, dtype=e4, device="cuda"))   # I = 256
+    bad_s = [torch.empty(8, 4, dtype=torch.bfloat16, device="cuda"),          # not fp32
+             torch.empty(8, 4, dtype=torch.float32),                          # on the host
+             torch.empty(8, 2, dtype=torch.float32, device="cuda")]           # too small
+    for s in bad_s:
+        with pytest.raises(ValueError, match="scales must be"):
+            fq.per_token_group_fp8_quant(x, scales=s)
+        with pytest.raises(ValueError, match="scales must be"):
+            fq.rms_norm_per_block_quant(x, w, scales=s)
+    with pytest.raises(ValueError, match="scales must be"):
+        fq.dynamic_per_token_scaled_fp8_quant(x, scales=torch.empty(8, 1, dtype=torch.float32))
+    with pytest.raises(ValueError, match="scales must be"):
+        fq.per_token_group_fp8_quant(x, ue8m0=True, packed_ue8m0_scales=True,
+                                     scales=torch.empty(fq.packed_scale_shape(8, 4), dtype=torch.int32))
+    with pytest.raises(ValueError):
+        fq.rms_norm_per_block_quant(x, w.cpu())
+    with pytest.raises(ValueError):
+        fq.rms_norm_per_block_quant(x, w, torch.zeros(8, 512, dtype=torch.bfloat16))
+    a = torch.zeros(16, device="cuda")
+    with pytest.raises(ValueError, match="out must be"):
+        fq.group_scale(a, out=torch.empty(8, device="cuda"))
+    with pytest.raises(ValueError, match="out must be"):
+        fq.f32_to_e4m3(a, out=torch.empty(16, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="out must be"):
+        fq.silu_mul(a, a, out=torch.empty(16, dtype=torch.float64, device="cuda"))
+    # nothing was launched on the rejected buffers; a good call still works
+    q, s = fq.per_token_group_fp8_quant(x)
+    torch.cuda.synchronize()
+    assert q.shape == (8, 512) and s.shape == (8, 4)
