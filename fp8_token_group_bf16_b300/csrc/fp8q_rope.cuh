@@ -24,10 +24,16 @@
 namespace fp8q {
 
 constexpr int kHeadDim = 128;
-// Two warps (16 heads) per CTA: at 80 registers a thread, 12 such CTAs fit
-// a SM.  Measured at T = 4096 with 64 + 8 heads: 28.0 us, against 28.9 us
-// with 128-thread and 30.1 us with 256-thread CTAs.
+// Two warps (16 heads) per CTA: at 72 registers a thread (the launch bounds
+// ask for 14 such CTAs per SM; the weights are loaded only after the head's
+// sum of squares, so they do not add to the registers live while it is
+// formed), 14 CTAs fit a SM.  Measured at T = 4096 with 64 + 8 heads, neox:
+// 26.8 us, against 28.0 us at 80 registers (12 CTAs per SM, weights loaded
+// with the head) and 29.8 us at 86; 72 registers with the weights loaded
+// with the head spill 56 bytes (28.6 us).  CTA size at 80 registers: 28.0 us
+// with 64-thread, 28.9 us with 128-thread, 30.1 us with 256-thread CTAs.
 constexpr int kRopeCtaThreads = 64;
+constexpr int kRopeMinCtas = 14;
 
 // 32 bytes (16 bf16) that this kernel also writes: coherent path.
 template <bool V8>
@@ -118,7 +124,7 @@ __device__ __forceinline__ void st_piece(uint16_t *p, const uint32_t *w)
 // Positions outside [0, P) are clamped into the table (the result for such
 // a token is unspecified, the access stays in bounds).
 template <int LPH, bool NEOX, bool V8>
-__global__ void __launch_bounds__(kRopeCtaThreads) qk_norm_rope_kernel(uint16_t *__restrict__ qkv,
+__global__ void __launch_bounds__(kRopeCtaThreads, kRopeMinCtas) qk_norm_rope_kernel(uint16_t *__restrict__ qkv,
                                                            const uint16_t *__restrict__ q_w,
                                                            const uint16_t *__restrict__ k_w,
                                                            const uint16_t *__restrict__ cos_sin,
@@ -147,14 +153,16 @@ __global__ void __launch_bounds__(kRopeCtaThreads) qk_norm_rope_kernel(uint16_t 
     int64_t pos = positions[t];
     pos = pos < 0 ? 0 : (pos >= P ? P - 1 : pos);
     const uint16_t *crow = cos_sin + pos * kHeadDim;
-    ld_piece_table<NWP, V8>(w + o0, wr);
-    ld_piece_table<NWP, V8>(w + o1, wr + NWP);
     ld_piece_table<NWP, V8>(crow + PIECE * sub, cs);                   // cos_j
     ld_piece_table<NWP, V8>(crow + kHeadDim / 2 + PIECE * sub, cs + NWP);   // sin_j
 
     // ---- 1/rms of the head: exact lane sums, TwoSum across the head's lanes
     float hi, lo;
     lane_sumsq(z, hi, lo);
+    // the weights (an L1 hit for all but the first heads of a SM), now that
+    // the sum's registers are free
+    ld_piece_table<NWP, V8>(w + o0, wr);
+    ld_piece_table<NWP, V8>(w + o1, wr + NWP);
 #pragma unroll
     for (int o = 1; o < LPH; o <<= 1)
         pair_add(hi, lo, __shfl_xor_sync(0xFFFFFFFFu, hi, o), __shfl_xor_sync(0xFFFFFFFFu, lo, o));
