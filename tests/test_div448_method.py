@@ -87,3 +87,23 @@ def test_division_by_448_is_correctly_rounded_for_every_significand():
     # both sides as (24-bit mantissa, exponent)
     bad = (Q != N) | (qe != te)
     assert not bad.any(), (int(bad.sum()), m[bad][:5])
+
+
+def test_ue8m0_scale_from_the_bits_of_amax():
+    """The kernels' UE8M0 scale skips the division: for a = m 2^e (m in
+    [1, 2)) the smallest power of two >= RN32(a / 448) is 2^(e - 8), doubled
+    when m > 1.75.  Checked exactly for every significand (the identity is
+    invariant under scaling a by powers of two while everything stays
+    normal): 2^j >= RN32(a / 448) must hold for the formula's j and fail for
+    j - 1."""
+    M = np.arange(1 << 23, dtype=np.int64)             # mantissa field; a = (2^23 + M) 2^-23
+    j = np.where(M > 0x600000, 1, 0) - 8                 # exponent of the scale, for e = 0
+    # RN32(a/448) <= 2^j  <=>  a/448 <= 2^j + ulp(2^j)/2 = 2^j (1 + 2^-24)  (ties go to the even 2^j)
+    #                     <=>  (2^23 + M) 2^-23 <= 448 2^j (1 + 2^-24)
+    #                     <=>  (2^23 + M) 2^25 <= 7 2^(j + 54) + 7 2^(j + 30)     [times 2^48]
+    lhs = (np.int64(1 << 23) + M) << 25
+
+    def bound(jj):
+        return 7 * ((np.int64(1) << (jj + 54)) + (np.int64(1) << (jj + 30)))
+    assert np.all(lhs <= bound(j))                       # 2^j is an upper bound
+    assert np.all(lhs > bound(j - 1))                    # 2^(j-1) is not
