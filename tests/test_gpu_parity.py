@@ -320,6 +320,23 @@ def test_rms_bit_exact(residual, ue8m0, col):
         assert np.array_equal(rout, ror)
 
 
+@pytest.mark.parametrize("residual", [False, True], ids=["plain", "residual"])
+def test_rms_single_wave_grids_alternating_block_sizes(residual):
+    """Rows of 4096, 5120 and 8192 values run one kernel with blocks of 128,
+    160 and 256 threads.  A grid that fits in one wave is spread evenly by
+    reserving shared memory per CTA, a different amount for each T and block
+    size; interleaving them checks that one size never leaves the kernel
+    allowed less than another size's launch asks for."""
+    for T, H in [(256, 4096), (512, 5120), (300, 8192), (256, 4096), (1000, 4096), (888, 5120), (512, 5120)]:
+        x, w, r = inputs.rms_input(T, H, seeds=(8100 + T, 8101 + H, 8102))
+        xb, wb, rb = inputs.bits(x), inputs.bits(w), inputs.bits(r) if residual else None
+        q, s, rout = gpu_rms(xb, wb, rb, True, False)
+        qr, sr, _, _, ror = oracle.rms_norm_per_block_quant(xb, wb, rb, ue8m0=True)
+        assert_exact(q, s, qr, sr, f"rms single wave T={T} H={H} residual={residual}")
+        if residual:
+            assert np.array_equal(rout, ror)
+
+
 @pytest.mark.parametrize("T,H", [(3, 24576), (512, 5120), (37, 1152), (2, 32768)])
 def test_rms_bit_exact_shapes(T, H):
     x = inputs.lognormal_channel_input(T, H, 6000 + T)
