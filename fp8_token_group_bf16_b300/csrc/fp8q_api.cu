@@ -14,7 +14,6 @@
 #include <map>
 #include <mutex>
 #include <tuple>
-#include <utility>
 #include <cuda_runtime.h>
 
 namespace {
@@ -95,109 +94,29 @@ int resident_per_sm(int threads, int regs)
     return std::min({32, 2048 / threads, 65536 / (regs * threads)});
 }
 
-// A per-device attribute of the current device, cached (0 if the query fails).
-int device_attr(cudaDeviceAttr attr)
-{
-    static std::atomic<int> cache[32][4];
-    const int slot = attr == cudaDevAttrMaxSharedMemoryPerMultiprocessor ? 0
-                     : attr == cudaDevAttrMaxSharedMemoryPerBlockOptin    ? 1
-                     : attr == cudaDevAttrReservedSharedMemoryPerBlock    ? 2
-                                                                          : 3;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
-        return 0;
-    const bool keep = dev >= 0 && dev < 32 && slot < 3;
-    int v = keep ? cache[dev][slot].load(std::memory_order_relaxed) : 0;
-    if (v == 0) {
-        if (cudaDeviceGetAttribute(&v, attr, dev) != cudaSuccess || v < 0)
-            return 0;
-        if (keep)
-            cache[dev][slot].store(v, std::memory_order_relaxed);
-    }
-    return v;
-}
-
-// One wave, spread evenly.  When a grid of `ctas` CTAs fits in one wave (the
-// SMs hold all of them at once), the CTA scheduler does not deal them out
-// evenly: rms_norm_per_block_quant at T = 512, H = 5120 (512 CTAs, 888
-// places) took 4.17 us, and 3.59 us when no SM could take more than
-// ceil(512 / 148) = 4 of them (H = 4096: 3.69 against 3.11 us; at T = 640,
-// 4.11 against 3.52 us); silu_and_mul_per_block_quant at T = 1024,
-// I = 2048: 4.13 against 3.51 us; fused_qk_norm_rope at T = 256 with 64 + 8
-// heads: 4.01 against 3.52 us.  (per_token_group_fp8_quant ran slower with
-// it and is launched without.)  The cap is set by reserving dynamic shared memory
-// the kernel never touches.  Returns the bytes to reserve, 0 for no cap
-// (more than one wave, a cap that would not bind, or a failed query), after
-// allowing the kernel that much.  Only grids small enough to be one wave
-// pay for the occupancy query.
+// CTAs of `threads` threads of `kernel` that one SM of the current device
+// holds at once (the occupancy query, cached per kernel, device and block
+// size); 0 if the query fails.
 template <typename... KArgs>
-size_t wave_cap_smem(void (*kernel)(KArgs...), int64_t ctas, int threads)
+int resident_ctas(void (*kernel)(KArgs...), int threads)
 {
-    const int sms = sm_count();
-    if (sms <= 0 || ctas > int64_t(sms) * 32)
-        return 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return 0;
-    // What the queries below return for this kernel and block size on this
-    // device, kept so that repeated calls skip them; and, per kernel and
-    // device (the attribute is the kernel's, whatever the block size), the
-    // dynamic shared memory the kernel is allowed so far.
-    struct Entry {
-        int resident;      // CTAs a SM holds without a cap
-        int64_t fixed;     // shared memory a CTA takes without dynamic memory
-    };
     static std::mutex mu;
-    static std::map<std::tuple<const void *, int, int>, Entry> known;
-    static std::map<std::pair<const void *, int>, int64_t> allowed;
-    const void *fn = reinterpret_cast<const void *>(kernel);
-    const auto key = std::make_tuple(fn, dev, threads);
-    Entry e;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        auto it = known.find(key);
-        if (it != known.end()) {
-            e = it->second;
-        } else {
-            cudaFuncAttributes fa;
-            e.resident = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&e.resident, kernel, threads, 0) != cudaSuccess ||
-                cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) {
-                cudaGetLastError();   // no cap; the launch reports its own status
-                return 0;
-            }
-            e.fixed = device_attr(cudaDevAttrReservedSharedMemoryPerBlock) + int64_t(fa.sharedSizeBytes);
-            known[key] = e;
-            allowed.emplace(std::make_pair(fn, dev), int64_t(fa.maxDynamicSharedSizeBytes));
-        }
-    }
-    if (e.resident <= 0 || ctas > int64_t(sms) * e.resident)
-        return 0;
-    const int cap = int((ctas + sms - 1) / sms);
-    if (cap < 2 || cap >= e.resident)
-        return 0;
-    const int per_sm = device_attr(cudaDevAttrMaxSharedMemoryPerMultiprocessor);
-    const int optin = device_attr(cudaDevAttrMaxSharedMemoryPerBlockOptin);
-    if (per_sm <= 0 || optin <= 0)
-        return 0;
-    // cap CTAs fit a SM's shared memory, cap + 1 do not
-    const int64_t per_cta = per_sm / cap - e.fixed - 256;
-    if (per_cta <= 0 || per_cta > optin || (cap + 1) * (per_cta + e.fixed) <= per_sm)
-        return 0;
-    // The attribute only ever grows (a smaller value would break a launch
-    // that another block size of the same kernel sized against a larger
-    // one).  It is a host-side attribute of the kernel on the current
-    // device, not a stream operation.
+    static std::map<std::tuple<const void *, int, int>, int> known;
+    const auto key = std::make_tuple(reinterpret_cast<const void *>(kernel), dev, threads);
     std::lock_guard<std::mutex> lock(mu);
-    int64_t &have = allowed[std::make_pair(fn, dev)];
-    if (per_cta > have) {
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(per_cta)) != cudaSuccess) {
-            cudaGetLastError();
-            return 0;
-        }
-        have = per_cta;
+    auto it = known.find(key);
+    if (it != known.end())
+        return it->second;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess) {
+        cudaGetLastError();   // no answer: the caller launches unpadded
+        return 0;
     }
-    return size_t(per_cta);
+    known[key] = n;
+    return n;
 }
 
 // Launch with programmatic stream serialization allowed: the kernel may be
@@ -239,13 +158,6 @@ cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t
     return launch_ex(kernel, grid, block, 1u, 0, st, args...);
 }
 
-// launch(), with a single-wave grid spread evenly (wave_cap_smem).
-template <typename... KArgs, typename... Args>
-cudaError_t launch_spread(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t st, Args... args)
-{
-    return launch_ex(kernel, grid, block, 1u, wave_cap_smem(kernel, int64_t(grid.x), int(block.x)), st, args...);
-}
-
 // Grid of a group kernel with Q groups per CTA (see group_of).
 template <bool TOKEN_MAJOR, int Q>
 dim3 group_grid(int64_t T, int64_t G)
@@ -256,8 +168,6 @@ dim3 group_grid(int64_t T, int64_t G)
 template <bool U, int C, bool V>
 cudaError_t launch_group(const uint16_t *x, uint8_t *q, float *s, int64_t G, int64_t T, float eps, cudaStream_t st)
 {
-    // (no wave cap: measured slower with one, 2.67 against 2.42 us at
-    // T = 256, H = 7168, UE8M0 column-major)
     return launch(group_quant_kernel<U, C, V>, group_grid<kGroupTokenMajor<U, C>, kGroupQuantGroupsPerCta>(T, G),
                   dim3{unsigned(kGroupCtaThreads)}, st, x, q, s, G, T, eps);
 }
@@ -266,8 +176,8 @@ template <bool U, int C, bool V>
 cudaError_t launch_silu(const uint16_t *x, uint8_t *q, float *s, int64_t G, int64_t T, int64_t I, float eps,
                         cudaStream_t st)
 {
-    return launch_spread(silu_quant_kernel<U, C, V>, group_grid<false, kSiluGroupsPerCta>(T, G),
-                         dim3{unsigned(kSiluCtaThreads)}, st, x, q, s, G, T, I, eps);
+    return launch(silu_quant_kernel<U, C, V>, group_grid<false, kSiluGroupsPerCta>(T, G),
+                  dim3{unsigned(kSiluCtaThreads)}, st, x, q, s, G, T, I, eps);
 }
 
 // rms_norm_per_block_quant, one CTA per row with the row in registers: one
@@ -288,8 +198,41 @@ cudaError_t launch_rms_row(const uint16_t *x, uint16_t *res, const uint16_t *w, 
             return launch(rms_row_kernel<NG, U, C, R, V, true>, grid, block, st, x, res, w, q, s, T, H, G, eps,
                           sms * 3 / 2);
     }
-    // a single wave: spread evenly over the SMs
-    return launch_spread(rms_row_kernel<NG, U, C, R, V, false>, grid, block, st, x, res, w, q, s, T, H, G, eps, 0);
+    // A single wave: spread evenly over the SMs.  The CTA scheduler does not
+    // deal a one-wave grid out evenly: some SMs take as many CTAs as fit while
+    // others idle.  With one group per quad the CTA is padded with warps that
+    // own no group (they leave at once, but their registers stay allocated)
+    // to the smallest block of which a SM holds ceil(T / SMs) = cap, for
+    // per-group scales, cap >= 3 and at most twice the threads that own
+    // groups.  Measured alone (us, padded against not): H = 5120, T = 512
+    // (6 CTAs of 160 threads fit a SM; padded to 256, 4 do) 3.94 / 4.19;
+    // H = 4096, T = 768 4.02 / 4.30; H = 8192, T = 300 3.71 / 4.24, with the
+    // residual 5.10 / 5.76; as op B of a chain of dependent launches (ops A,
+    // B, C at T = 512) 3.76 / 4.28.  Not padded: cap 2 (H = 8192, T = 256
+    // 3.62 / 3.52; to 512 threads at H = 5120 2.84 / 2.75) and the per-token
+    // scale, whose second row barrier made it slower (H = 4096, T = 512:
+    // 4.63 / 3.73).
+    // Reserving unused shared memory per CTA to the same end measured faster
+    // alone (3.61 us) but slower in the chain (5.61 us): a SM must drain
+    // before its shared-memory configuration changes, so the launch no
+    // longer overlapped its predecessor's drain.
+    auto k = rms_row_kernel<NG, U, C, R, V, false>;
+    unsigned block_x = unsigned(threads);
+    const int sms = sm_count(), fit = sms > 0 ? resident_ctas(k, threads) : 0;
+    if (fit > 0 && int64_t(T) <= int64_t(sms) * fit) {
+        const int cap = (T + sms - 1) / sms;
+        if (C != kPerToken && cap >= 3 && cap < fit) {
+            for (int t = threads + 32; t <= std::min(kRmsBlockMax<NG>, 2 * threads); t += 32) {
+                const int r = resident_ctas(k, t);
+                if (r <= cap) {
+                    if (r == cap)
+                        block_x = unsigned(t);
+                    break;
+                }
+            }
+        }
+    }
+    return launch(k, grid, dim3{block_x}, st, x, res, w, q, s, T, H, G, eps, 0);
 }
 
 // rms_norm_per_block_quant for at most kRmsSplitMaxRows rows of more than 64
@@ -615,8 +558,8 @@ int fp8q_fused_qk_norm_rope(void *qkv, const void *q_weight, const void *k_weigh
     auto st = static_cast<cudaStream_t>(stream);
     const int nhi = int(nh), hq = int(num_q_heads);
     cudaError_t e;
-#define FP8Q_ROPE(N, V) launch_spread(qk_norm_rope_kernel<kLph, N, V>, grid, block, st, x, qw, kw, cs, positions, n, \
-                                      nhi, hq, row, max_position, eps)
+#define FP8Q_ROPE(N, V) launch(qk_norm_rope_kernel<kLph, N, V>, grid, block, st, x, qw, kw, cs, positions, n, nhi, hq, \
+                               row, max_position, eps)
     if (is_neox)
         e = v8 ? FP8Q_ROPE(true, true) : FP8Q_ROPE(true, false);
     else

@@ -21,11 +21,25 @@
 
 namespace fp8q {
 
+// Threads that own groups: at most 64 quads.
 constexpr int kRmsMaxThreads = 256;
-// CTAs per SM the launch bounds ask for (and so the register cap): NG groups
-// per quad hold 32 NG values and as many weights in registers.
+// CTAs of kRmsMaxThreads per SM that the register cap allows: NG groups per
+// quad hold 32 NG values and as many weights in registers (64, 128 and 255
+// registers a thread).
 template <int NG>
 constexpr int kRmsMinCtas = NG == 1 ? 4 : (NG == 2 ? 2 : 1);
+// The largest block the host may launch: with one group per quad it may pad
+// a CTA with warps that own no group, so that fewer CTAs fit a SM (the
+// launch bounds keep the same register cap).
+template <int NG>
+constexpr int kRmsBlockMax = NG == 1 ? 2 * kRmsMaxThreads : kRmsMaxThreads;
+
+// bar.sync on barrier 1 for the first n threads of the CTA (n a multiple of
+// 32); the same memory ordering among them as __syncthreads().
+__device__ __forceinline__ void bar_sync_first(int n)
+{
+    asm volatile("bar.sync 1, %0;" ::"r"(n) : "memory");
+}
 
 // Squares of one lane's 2*NW values (NW bf16x2 words, NW even), summed
 // exactly: returns (hi, lo) with hi + lo equal to the sum up to lo's own
@@ -97,14 +111,19 @@ __device__ __forceinline__ float rms_inv(float hi, float lo, int H, float eps)
 // and w after the barrier.
 
 template <int NG, bool UE8M0, int LAYOUT, bool RES, bool V8, bool PF>
-__global__ void __launch_bounds__(kRmsMaxThreads, kRmsMinCtas<NG>) rms_row_kernel(
-    const uint16_t *__restrict__ x, uint16_t *__restrict__ residual, const uint16_t *__restrict__ w,
-    uint8_t *__restrict__ q, float *__restrict__ scales, int T, int H, int G, float eps, int pf)
+__global__ void __launch_bounds__(kRmsBlockMax<NG>, kRmsMinCtas<NG> * kRmsMaxThreads / kRmsBlockMax<NG>)
+    rms_row_kernel(const uint16_t *__restrict__ x, uint16_t *__restrict__ residual, const uint16_t *__restrict__ w,
+                   uint8_t *__restrict__ q, float *__restrict__ scales, int T, int H, int G, float eps, int pf)
 {
     __shared__ float2 red[kRmsMaxThreads / 32];
     __shared__ float redm[kRmsMaxThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, sub = tid & 3, quad = tid >> 2, warp = tid >> 5;
-    const int nq = blockDim.x >> 2, nwarps = blockDim.x >> 5;
+    // the threads that own groups: ceil(G / NG) quads, in whole warps; warps
+    // beyond them only pad the CTA and leave at once
+    const int nthr = (((G + NG - 1) / NG * 4 + 31) >> 5) << 5;
+    if (tid >= nthr)
+        return;
+    const int nq = nthr >> 2, nwarps = nthr >> 5;
     const int row = blockIdx.x;
     const int64_t rbase = int64_t(row) * H;
 
@@ -156,7 +175,7 @@ __global__ void __launch_bounds__(kRmsMaxThreads, kRmsMinCtas<NG>) rms_row_kerne
         pair_add(hi, lo, __shfl_xor_sync(0xFFFFFFFFu, hi, o), __shfl_xor_sync(0xFFFFFFFFu, lo, o));
     if (lane == 0)
         red[warp] = make_float2(hi, lo);
-    __syncthreads();
+    bar_sync_first(nthr);
     float2 a = red[0];
     for (int i = 1; i < nwarps; ++i)   // every thread, in the same order
         pair_add(a.x, a.y, red[i].x, red[i].y);
@@ -185,7 +204,7 @@ __global__ void __launch_bounds__(kRmsMaxThreads, kRmsMinCtas<NG>) rms_row_kerne
             m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
         if (lane == 0)
             redm[warp] = m;
-        __syncthreads();
+        bar_sync_first(nthr);
         float amax = redm[0];
         for (int i = 1; i < nwarps; ++i)
             amax = fmaxf(amax, redm[i]);

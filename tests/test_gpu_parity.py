@@ -324,10 +324,13 @@ def test_rms_bit_exact(residual, ue8m0, col):
 def test_rms_single_wave_grids_alternating_block_sizes(residual):
     """Rows of 4096, 5120 and 8192 values run one kernel with blocks of 128,
     160 and 256 threads.  A grid that fits in one wave is spread evenly by
-    reserving shared memory per CTA, a different amount for each T and block
-    size; interleaving them checks that one size never leaves the kernel
-    allowed less than another size's launch asks for."""
-    for T, H in [(256, 4096), (512, 5120), (300, 8192), (256, 4096), (1000, 4096), (888, 5120), (512, 5120)]:
+    padding its CTAs with warps that own no group (T = 512, 300, 444 and
+    768 here: 256, 320, 320 and 160 threads), which leave at once and must
+    neither hold up the row barrier nor write; T = 256, 1000 and 888 are not
+    padded.  Interleaving the sizes checks that each launch takes its own
+    block."""
+    for T, H in [(256, 4096), (512, 5120), (300, 8192), (256, 4096), (1000, 4096), (888, 5120), (444, 5120),
+                 (768, 4096), (512, 5120)]:
         x, w, r = inputs.rms_input(T, H, seeds=(8100 + T, 8101 + H, 8102))
         xb, wb, rb = inputs.bits(x), inputs.bits(w), inputs.bits(r) if residual else None
         q, s, rout = gpu_rms(xb, wb, rb, True, False)

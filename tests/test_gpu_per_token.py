@@ -124,6 +124,8 @@ def _token_rms(xb, wb, rb, ue8m0):
 @pytest.mark.parametrize("T,H,residual", [(1, 128, False), (7, 896, True), (256, 4096, False),
                                           (256, 4096, True), (3, 24576, False), (2, 32768, True),
                                           (5, 16384, False), (512, 5120, True), (2048, 5120, False),
+                                          # one-wave grids (per-group scales would pad these CTAs)
+                                          (512, 5120, False), (300, 8192, False),
                                           # the prefetching builds of the 2- and 4-groups-per-quad rows
                                           (400, 12288, False), (200, 20480, False)])
 @pytest.mark.parametrize("ue8m0", [False, True], ids=["fp32", "ue8m0"])
