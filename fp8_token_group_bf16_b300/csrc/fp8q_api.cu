@@ -186,18 +186,30 @@ template <int NG, bool U, int C, bool R, bool V>
 cudaError_t launch_rms_row(const uint16_t *x, uint16_t *res, const uint16_t *w, uint8_t *q, float *s, int T,
                            int H, int G, float eps, cudaStream_t st)
 {
+    // rows of at most kRmsWarpRowGroups groups: a warp each, kRmsWarpRowsPerCta
+    // rows per CTA; longer rows: a CTA each
+    const bool wpr = NG == 1 && G <= kRmsWarpRowGroups;
+    const int rpc = wpr ? kRmsWarpRowsPerCta : 1;
     const int quads = (G + NG - 1) / NG;
-    const int threads = ((quads * 4 + 31) / 32) * 32;
-    const dim3 grid{unsigned(T)}, block{unsigned(threads)};
-    // The prefetching build, at a distance of 1.5 x the SM count, when rows
-    // wait for a later wave (more rows than CTAs resident at once), without
-    // the residual.
+    const int threads = wpr ? 32 * rpc : ((quads * 4 + 31) / 32) * 32;
+    const dim3 grid{unsigned((T + rpc - 1) / rpc)}, block{unsigned(threads)};
+    // The prefetching build, at a distance of 1.5 x the SM count in CTAs,
+    // when rows wait for a later wave (more rows than resident at once),
+    // without the residual.
     if constexpr (!R) {
         const int sms = sm_count();
-        if (int64_t(T) > int64_t(sms) * resident_per_sm(threads, 65536 / (kRmsMaxThreads * kRmsMinCtas<NG>)))
+        if (int64_t(T) >
+            int64_t(sms) * rpc * resident_per_sm(threads, 65536 / (kRmsMaxThreads * kRmsMinCtas<NG>))) {
+            if (wpr)
+                return launch(rms_row_kernel<NG, U, C, R, V, true, NG == 1>, grid, block, st, x, res, w, q, s, T, H,
+                              G, eps, sms * 3 / 2 * rpc);
             return launch(rms_row_kernel<NG, U, C, R, V, true>, grid, block, st, x, res, w, q, s, T, H, G, eps,
                           sms * 3 / 2);
+        }
     }
+    if (wpr)
+        return launch(rms_row_kernel<NG, U, C, R, V, false, NG == 1>, grid, block, st, x, res, w, q, s, T, H, G,
+                      eps, 0);
     // A single wave: spread evenly over the SMs.  The CTA scheduler does not
     // deal a one-wave grid out evenly: some SMs take as many CTAs as fit while
     // others idle.  With one group per quad the CTA is padded with warps that

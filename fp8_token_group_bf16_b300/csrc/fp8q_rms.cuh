@@ -33,6 +33,9 @@ constexpr int kRmsMinCtas = NG == 1 ? 4 : (NG == 2 ? 2 : 1);
 // launch bounds keep the same register cap).
 template <int NG>
 constexpr int kRmsBlockMax = NG == 1 ? 2 * kRmsMaxThreads : kRmsMaxThreads;
+// Rows of at most this many groups take a warp each, this many rows per CTA.
+constexpr int kRmsWarpRowGroups = 8;
+constexpr int kRmsWarpRowsPerCta = 4;
 
 // bar.sync on barrier 1 for the first n threads of the CTA (n a multiple of
 // 32); the same memory ordering among them as __syncthreads().
@@ -91,7 +94,10 @@ __device__ __forceinline__ float rms_inv(float hi, float lo, int H, float eps)
 // warp reduces its lanes' exact partial sums with a butterfly; one barrier
 // joins the warps.  The weight is read through L1 (every CTA of a SM reads
 // the same bytes).  Short-lived CTAs at ~64 registers leave room for six per
-// SM, whose loads overlap the others' arithmetic.
+// SM, whose loads overlap the others' arithmetic.  A row of at most 8 groups
+// fits one warp: it then takes a warp of a CTA of several rows and needs
+// neither shared memory nor a barrier (one CTA per such short row would make
+// the CTA launch rate the limit).
 //
 // While a CTA waits on its barrier, its loads are done and it asks nothing of
 // HBM.  When the grid is longer than the CTAs resident at once, the PF
@@ -110,21 +116,26 @@ __device__ __forceinline__ float rms_inv(float hi, float lo, int H, float eps)
 // against 20.0 us at T = 4096, H = 5120 for forming v a second time from z
 // and w after the barrier.
 
-template <int NG, bool UE8M0, int LAYOUT, bool RES, bool V8, bool PF>
+template <int NG, bool UE8M0, int LAYOUT, bool RES, bool V8, bool PF, bool WPR = false>
 __global__ void __launch_bounds__(kRmsBlockMax<NG>, kRmsMinCtas<NG> * kRmsMaxThreads / kRmsBlockMax<NG>)
     rms_row_kernel(const uint16_t *__restrict__ x, uint16_t *__restrict__ residual, const uint16_t *__restrict__ w,
                    uint8_t *__restrict__ q, float *__restrict__ scales, int T, int H, int G, float eps, int pf)
 {
     __shared__ float2 red[kRmsMaxThreads / 32];
     __shared__ float redm[kRmsMaxThreads / 32];
-    const int tid = threadIdx.x, lane = tid & 31, sub = tid & 3, quad = tid >> 2, warp = tid >> 5;
-    // the threads that own groups: ceil(G / NG) quads, in whole warps; warps
-    // beyond them only pad the CTA and leave at once
-    const int nthr = (((G + NG - 1) / NG * 4 + 31) >> 5) << 5;
-    if (tid >= nthr)
+    const int tid = threadIdx.x, lane = tid & 31, sub = tid & 3, warp = tid >> 5;
+    // WPR (rows of at most kRmsWarpRowGroups groups): a warp per row,
+    // blockDim.x / 32 rows per CTA.  Otherwise a CTA per row, whose threads
+    // that own groups are ceil(G / NG) quads in whole warps; warps beyond
+    // them only pad the CTA and leave at once.
+    static_assert(!WPR || NG == 1, "a warp holds one group per quad");
+    constexpr bool wpr = WPR;
+    const int nthr = wpr ? 32 : (((G + NG - 1) / NG * 4 + 31) >> 5) << 5;
+    const int row = wpr ? int(blockIdx.x) * int(blockDim.x >> 5) + warp : int(blockIdx.x);
+    if ((!wpr && tid >= nthr) || row >= T)
         return;
+    const int quad = (wpr ? lane : tid) >> 2;
     const int nq = nthr >> 2, nwarps = nthr >> 5;
-    const int row = blockIdx.x;
     const int64_t rbase = int64_t(row) * H;
 
     wait_for_producer();
@@ -149,7 +160,7 @@ __global__ void __launch_bounds__(kRmsBlockMax<NG>, kRmsMinCtas<NG> * kRmsMaxThr
     // will take it.
     if constexpr (PF) {
         static_assert(!RES, "no prefetch with the residual");
-        if (tid == 0 && row + pf < T)
+        if ((wpr ? lane : tid) == 0 && row + pf < T)
             prefetch_l2_bulk(x + rbase + int64_t(pf) * H, uint32_t(H) * 2);
     }
     if (RES) {
@@ -173,12 +184,18 @@ __global__ void __launch_bounds__(kRmsBlockMax<NG>, kRmsMinCtas<NG> * kRmsMaxThr
 #pragma unroll
     for (int o = 1; o <= 16; o <<= 1)
         pair_add(hi, lo, __shfl_xor_sync(0xFFFFFFFFu, hi, o), __shfl_xor_sync(0xFFFFFFFFu, lo, o));
-    if (lane == 0)
-        red[warp] = make_float2(hi, lo);
-    bar_sync_first(nthr);
-    float2 a = red[0];
-    for (int i = 1; i < nwarps; ++i)   // every thread, in the same order
-        pair_add(a.x, a.y, red[i].x, red[i].y);
+    // One warp: every lane holds the same pair (pair_add is symmetric, so both
+    // partners of each butterfly step form the same sum).  Several: one
+    // barrier, then every thread adds the warps' pairs in the same order.
+    float2 a = make_float2(hi, lo);
+    if (nwarps > 1) {
+        if (lane == 0)
+            red[warp] = a;
+        bar_sync_first(nthr);
+        a = red[0];
+        for (int i = 1; i < nwarps; ++i)
+            pair_add(a.x, a.y, red[i].x, red[i].y);
+    }
     const float inv = rms_inv(a.x, a.y, H, eps);
     const uint64_t inv2 = f2_pack(inv, inv);
 
@@ -202,12 +219,15 @@ __global__ void __launch_bounds__(kRmsBlockMax<NG>, kRmsMinCtas<NG> * kRmsMaxThr
 #pragma unroll
         for (int o = 1; o <= 16; o <<= 1)
             m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-        if (lane == 0)
-            redm[warp] = m;
-        bar_sync_first(nthr);
-        float amax = redm[0];
-        for (int i = 1; i < nwarps; ++i)
-            amax = fmaxf(amax, redm[i]);
+        float amax = m;
+        if (nwarps > 1) {
+            if (lane == 0)
+                redm[warp] = m;
+            bar_sync_first(nthr);
+            amax = redm[0];
+            for (int i = 1; i < nwarps; ++i)
+                amax = fmaxf(amax, redm[i]);
+        }
         const float sc = group_scale<UE8M0>(amax, kScaleFloor);
         const float rc = scale_recip<UE8M0>(sc);
 
@@ -223,7 +243,7 @@ __global__ void __launch_bounds__(kRmsBlockMax<NG>, kRmsMinCtas<NG> * kRmsMaxThr
             if (g < G)
                 st32<V8>(q + rbase + g * kGroup + sub * kValsPerLane, codes);
         }
-        if (tid == 0)
+        if ((wpr ? lane : tid) == 0)
             scales[row] = sc;
     } else {
         // ---- pass 2: v = (z * inv) * w, group scale, codes
