@@ -20,10 +20,6 @@ namespace {
 
 using namespace fp8q;
 
-#ifndef FP8Q_ROPE_LANES
-#define FP8Q_ROPE_LANES 4
-#endif
-
 static_assert(FP8Q_TOKEN_MAX_COLS == kTokenMaxGroups * kGroup, "per-token row limit");
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -289,6 +285,35 @@ cudaError_t launch_rms(const uint16_t *x, uint16_t *res, const uint16_t *w, uint
         return FP8Q_ROW(2);
     return FP8Q_ROW(4);
 #undef FP8Q_ROW
+}
+
+// fused_qk_norm_rope: LPH lanes per (token, head) unit, kRopeCtaThreads / LPH
+// units per CTA.  Four lanes a head (32 values each), or eight (16 values,
+// 60 registers, 17 CTAs per SM) when that grid fits in one wave: measured
+// with 64 + 8 heads (neox), eight against four lanes: T = 16 1.28 / 1.54 us,
+// T = 128 2.72 / 2.95, T = 256 3.34 / 4.03; past one wave four lanes win
+// (T = 384 4.75 / 4.35, T = 4096 38.8 / 26.8).  Both are bit-identical.
+template <int LPH, bool N, bool V>
+cudaError_t launch_rope_lanes(uint16_t *x, const uint16_t *qw, const uint16_t *kw, const uint16_t *cs,
+                              const int64_t *positions, int64_t n, int nh, int hq, int64_t row, int64_t P, float eps,
+                              cudaStream_t st)
+{
+    constexpr int upc = kRopeCtaThreads / LPH;
+    return launch(qk_norm_rope_kernel<LPH, N, V>, dim3{unsigned((n + upc - 1) / upc)},
+                  dim3{unsigned(kRopeCtaThreads)}, st, x, qw, kw, cs, positions, n, nh, hq, row, P, eps);
+}
+
+template <bool N, bool V>
+cudaError_t launch_rope(uint16_t *x, const uint16_t *qw, const uint16_t *kw, const uint16_t *cs,
+                        const int64_t *positions, int64_t n, int nh, int hq, int64_t row, int64_t P, float eps,
+                        cudaStream_t st)
+{
+    constexpr int upc8 = kRopeCtaThreads / 8;
+    const int sms = sm_count();
+    const int fit = sms > 0 ? resident_ctas(qk_norm_rope_kernel<8, N, V>, kRopeCtaThreads) : 0;
+    if (fit > 0 && (n + upc8 - 1) / upc8 <= int64_t(sms) * fit)
+        return launch_rope_lanes<8, N, V>(x, qw, kw, cs, positions, n, nh, hq, row, P, eps, st);
+    return launch_rope_lanes<4, N, V>(x, qw, kw, cs, positions, n, nh, hq, row, P, eps, st);
 }
 
 // Per-token ops A and C: C CTAs per row (a cluster when C > 1), gpc =
@@ -564,14 +589,10 @@ int fp8q_fused_qk_norm_rope(void *qkv, const void *q_weight, const void *k_weigh
     auto qw = static_cast<const uint16_t *>(q_weight);
     auto kw = static_cast<const uint16_t *>(k_weight);
     auto cs = static_cast<const uint16_t *>(cos_sin);
-    constexpr int kLph = FP8Q_ROPE_LANES;   // lanes per head
-    constexpr int kUpc = kRopeCtaThreads / kLph;   // units per CTA
-    const dim3 grid{unsigned((n + kUpc - 1) / kUpc)}, block{unsigned(kRopeCtaThreads)};
     auto st = static_cast<cudaStream_t>(stream);
     const int nhi = int(nh), hq = int(num_q_heads);
     cudaError_t e;
-#define FP8Q_ROPE(N, V) launch(qk_norm_rope_kernel<kLph, N, V>, grid, block, st, x, qw, kw, cs, positions, n, nhi, hq, \
-                               row, max_position, eps)
+#define FP8Q_ROPE(N, V) launch_rope<N, V>(x, qw, kw, cs, positions, n, nhi, hq, row, max_position, eps, st)
     if (is_neox)
         e = v8 ? FP8Q_ROPE(true, true) : FP8Q_ROPE(true, false);
     else

@@ -2,7 +2,12 @@
 
 Every step is one correctly rounded fp32 operation in the oracle's order and
 the head's sum of squares is exact, so the bf16 outputs must be identical,
-value heads included (they must come back untouched)."""
+value heads included (they must come back untouched).
+
+A grid that fits in one wave with eight lanes a head takes that build (up
+to a few hundred tokens of 64 + 8 heads; here T <= 256), larger ones four
+lanes a head (T = 600, 1000, 4096 here); both pairings and both load widths
+are covered for each."""
 
 import numpy as np
 import pytest
@@ -54,9 +59,10 @@ def test_qk_norm_rope_exact(T, Hq, Hkv, is_neox):
     _check(T, Hq, Hkv, is_neox, seed=6100 + T + Hq)
 
 
+@pytest.mark.parametrize("T,Hq,Hkv", [(9, 8, 2), (600, 64, 8)])
 @pytest.mark.parametrize("is_neox", [True, False], ids=["neox", "interleaved"])
-def test_qk_norm_rope_16_byte_aligned(is_neox):
-    _check(9, 8, 2, is_neox, seed=6200, offset_bytes=16)
+def test_qk_norm_rope_16_byte_aligned(T, Hq, Hkv, is_neox):
+    _check(T, Hq, Hkv, is_neox, seed=6200 + T, offset_bytes=16)
 
 
 def test_qk_norm_rope_table_ends_and_repeats():
