@@ -820,6 +820,21 @@ def sweep(args):
     fq.load()
     dev = torch.device("cuda")
     peak, peak_kind = load_peaks()
+    clocks = ClockSampler(torch.cuda.current_device()).start()
+    try:
+        t0 = time.perf_counter()
+        rows = _sweep_points(fq, dev, peak, peak_kind)
+        t1 = time.perf_counter()
+    finally:
+        clocks.stop()
+    # one line for the whole sweep: the SM clock and clock-event reasons over its replays
+    print(json.dumps({"sweep_clocks": clocks.summary(t0, t1)}), flush=True)
+    return rows
+
+
+def _sweep_points(fq, dev, peak, peak_kind):
+    import torch
+
     timed = graph_time_us
 
     e4 = torch.float8_e4m3fn
@@ -833,6 +848,8 @@ def sweep(args):
     points.append(("rms_norm_per_block_quant", 256, 4096, False, "row", True))
     points.append(("rms_norm_per_block_quant", 256, 4096, False, "row", False))
     points.append(("silu_and_mul_per_block_quant", 1024, 12288, True, "col", False))
+    for T in (4096, 16384):   # short rows: a warp per row
+        points.append(("rms_norm_per_block_quant", T, 1024, True, "row", False))
     for T in (512, 4096):   # packed UE8M0 exponent bytes, and the same bytes in MXFP8 GEMM tiles
         for lay in ("packed", "mx"):
             points.append(("per_token_group_fp8_quant", T, A_H, True, lay, False))
@@ -891,7 +908,7 @@ def sweep(args):
     table = _inputs.rotary_table(_inputs.QK_P).to(dev)
     qw = (1.0 + 0.1 * torch.randn(128, device=dev)).to(torch.bfloat16)
     kw = (1.0 + 0.1 * torch.randn(128, device=dev)).to(torch.bfloat16)
-    for T in (64, 512, 4096, 16384):
+    for T in (64, 256, 512, 4096, 16384):
         nbytes = qk_rope_bytes(T)
 
         def make(T=T):
