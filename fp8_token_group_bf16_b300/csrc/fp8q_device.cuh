@@ -361,6 +361,14 @@ __device__ __forceinline__ uint64_t f2_from_bf16x2(uint32_t w)
     return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
+// The same, each half negated when NEG (a sign-bit flip, exact).
+template <bool NEG>
+__device__ __forceinline__ uint64_t f2_from_bf16x2_neg(uint32_t w)
+{
+    constexpr uint32_t f = NEG ? 0x80000000u : 0u;
+    return f2_pack(__uint_as_float((w << 16) ^ f), __uint_as_float((w & 0xFFFF0000u) ^ f));
+}
+
 // max(|a|, |b|, |c|) in one three-input instruction.
 __device__ __forceinline__ float absmax3(float m, float a, float b)
 {
@@ -414,43 +422,45 @@ __device__ __forceinline__ uint32_t pack4_e4m3(float a0, float a1, float a2, flo
 
 // Quantise 8 values (four packed pairs) with their group's scale s and
 // r = scale_recip(s) into 8 codes (c0: values 0-3, c1: values 4-7): each
-// code is e4m3(RN32(v / s)), the quotient correctly rounded.
+// code is e4m3(RN32(v / s)), the quotient correctly rounded.  The caller
+// passes w = v for a power-of-two scale (UE8M0) and w = -v otherwise (a sign
+// flip it gets for free or nearly: a negated factor, or bf16 inputs converted
+// with their sign bits flipped, f2_from_bf16x2_neg).
 //
-// Power-of-two s (UE8M0): r is exactly 1/s, so one multiply is the exact
-// quotient rounded once (its sign, zero included, is the sign of v).
-// Otherwise: y0 = RN(v r) is within 1.5 ulp of v/s; one residual step
-// y1 = RN(y0 + RN(v - s y0) r) makes it faithful; a second step with the
+// Power-of-two s: r is exactly 1/s, so one multiply is the exact quotient
+// rounded once (its sign, zero included, is the sign of v).
+// Otherwise: y0 = RN(v r) = RN(w (-r)) is within 1.5 ulp of v/s; one residual
+// step y1 = RN(y0 + RN(v - s y0) r) makes it faithful; a second step with the
 // exact residual v - s y1 (an FMA) then yields RN32(v/s) by Markstein's
 // theorem (P. Markstein, "Computation of elementary functions on the IBM
 // RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990: a faithful
 // quotient corrected with a correctly rounded reciprocal and an exact FMA
 // residual is the correctly rounded quotient, barring underflow).  Underflow
 // only happens for quotients far below 2^-10, whose e4m3 code is zero either
-// way.  Rounding to nearest is symmetric, so the steps run on signed values;
-// the sign of v, which a zero quotient can lose, is put back last.
+// way.  Each step is taken as e = RN(s y + w) = -RN(v - s y) and
+// y' = RN(y + e (-r)), the same values (RN is symmetric), in an order that
+// keeps the sign of a zero quotient: for v = -0 (w = +0), y0 = -0,
+// e = RN(s (-0) + 0) = +0 and y' = RN(+0 (-r) + (-0)) = -0; for v = +0
+// every step gives +0; a quotient that underflows keeps the sign of v.
 template <bool UE8M0>
-__device__ __forceinline__ void quant8(const uint64_t (&v)[4], float s, float r, uint32_t &c0, uint32_t &c1)
+__device__ __forceinline__ void quant8(const uint64_t (&w)[4], float s, float r, uint32_t &c0, uint32_t &c1)
 {
     float q[8];
     if (UE8M0) {
         const uint64_t r2 = f2_pack(r, r);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-            f2_unpack(f2_mul(v[k], r2), q[2 * k], q[2 * k + 1]);
+            f2_unpack(f2_mul(w[k], r2), q[2 * k], q[2 * k + 1]);
     } else {
-        const uint64_t r2 = f2_pack(r, r), ns2 = f2_pack(-s, -s);
+        const uint64_t nr2 = f2_pack(-r, -r), s2 = f2_pack(s, s);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            uint64_t y = f2_mul(v[k], r2);
-            uint64_t e = f2_fma(y, ns2, v[k]);
-            y = f2_fma(e, r2, y);
-            e = f2_fma(y, ns2, v[k]);
-            y = f2_fma(e, r2, y);
-            float vl, vh;
-            f2_unpack(v[k], vl, vh);
+            uint64_t y = f2_mul(w[k], nr2);
+            uint64_t e = f2_fma(s2, y, w[k]);
+            y = f2_fma(e, nr2, y);
+            e = f2_fma(s2, y, w[k]);
+            y = f2_fma(e, nr2, y);
             f2_unpack(y, q[2 * k], q[2 * k + 1]);
-            q[2 * k] = copysignf(q[2 * k], vl);
-            q[2 * k + 1] = copysignf(q[2 * k + 1], vh);
         }
     }
     c0 = pack4_e4m3(q[0], q[1], q[2], q[3]);

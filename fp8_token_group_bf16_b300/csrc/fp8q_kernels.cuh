@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(kGroupCtaThreads) group_quant_kernel(const uin
     float m = 0.0f;
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-        v[k] = f2_from_bf16x2(raw[k]);
+        v[k] = f2_from_bf16x2_neg<!UE8M0>(raw[k]);   // v, or -v for quant8
         m = absmax3(m, bf_lo(raw[k]), bf_hi(raw[k]));
     }
     const float amax = quad_max(m);
@@ -197,9 +197,12 @@ __device__ __forceinline__ uint64_t silu_mul_f2(uint64_t a, uint64_t b)
     return f2_mul(q, b);
 }
 
+// SiLU(a) * b from bf16x2 words; with NEG, SiLU(a) * (-b), the negated
+// product (exactly: RN is symmetric).
+template <bool NEG = false>
 __device__ __forceinline__ uint64_t silu_mul2(uint32_t aw, uint32_t bw)
 {
-    return silu_mul_f2(f2_from_bf16x2(aw), f2_from_bf16x2(bw));
+    return silu_mul_f2(f2_from_bf16x2(aw), f2_from_bf16x2_neg<NEG>(bw));
 }
 
 template <bool UE8M0, int LAYOUT, bool V8>
@@ -223,7 +226,7 @@ __global__ void __launch_bounds__(kSiluCtaThreads, 16) silu_quant_kernel(const u
     float m = 0.0f;
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-        v[k] = silu_mul2(ra[k], rb[k]);
+        v[k] = silu_mul2<!UE8M0>(ra[k], rb[k]);   // v, or -v for quant8
         float v0, v1;
         f2_unpack(v[k], v0, v1);
         m = absmax3(m, v0, v1);

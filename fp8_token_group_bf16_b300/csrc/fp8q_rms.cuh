@@ -197,7 +197,9 @@ __global__ void __launch_bounds__(kRmsBlockMax<NG>, kRmsMinCtas<NG> * kRmsMaxThr
             pair_add(a.x, a.y, red[i].x, red[i].y);
     }
     const float inv = rms_inv(a.x, a.y, H, eps);
-    const uint64_t inv2 = f2_pack(inv, inv);
+    // With an fp32 scale the normalised values are formed negated (exactly:
+    // RN is symmetric), as quant8 takes them; the maxima take |v| either way.
+    const uint64_t inv2 = UE8M0 ? f2_pack(inv, inv) : f2_pack(-inv, -inv);
 
     if constexpr (LAYOUT == kPerToken) {
         // ---- pass 2: v = (z * inv) * w, in the registers z and w free, and its row maximum

@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(kRmsMaxThreads) rms_split_kernel(
     for (int r = 1; r < C; ++r)
         pair_add(s.x, s.y, part[r].x, part[r].y);
     const float inv = rms_inv(s.x, s.y, H, eps);
-    const uint64_t inv2 = f2_pack(inv, inv);
+    const uint64_t inv2 = UE8M0 ? f2_pack(inv, inv) : f2_pack(-inv, -inv);   // v, or -v for quant8
 
     // v = (z * inv) * w, group scale, codes
     uint64_t v[4][4];

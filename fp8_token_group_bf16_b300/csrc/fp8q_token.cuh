@@ -158,8 +158,9 @@ __global__ void __launch_bounds__(kCtaThreads, kTokenQuantMinCtas) token_quant_k
     uint32_t codes[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const uint64_t v[4] = {f2_from_bf16x2(raw[4 * i]), f2_from_bf16x2(raw[4 * i + 1]),
-                               f2_from_bf16x2(raw[4 * i + 2]), f2_from_bf16x2(raw[4 * i + 3])};
+        constexpr bool neg = !UE8M0;   // v, or -v for quant8
+        const uint64_t v[4] = {f2_from_bf16x2_neg<neg>(raw[4 * i]), f2_from_bf16x2_neg<neg>(raw[4 * i + 1]),
+                               f2_from_bf16x2_neg<neg>(raw[4 * i + 2]), f2_from_bf16x2_neg<neg>(raw[4 * i + 3])};
         quant8<UE8M0>(v, s, rc, codes[2 * i], codes[2 * i + 1]);
     }
     if (act)
@@ -220,7 +221,7 @@ __global__ void __launch_bounds__(kCtaThreads, kTokenSiluMinCtas) token_silu_ker
     float m = 0.0f;
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-        v[k] = silu_mul2(ra[k], rb[k]);
+        v[k] = silu_mul2<!UE8M0>(ra[k], rb[k]);   // v, or -v for quant8
         float v0, v1;
         f2_unpack(v[k], v0, v1);
         m = absmax3(m, v0, v1);

@@ -340,6 +340,36 @@ def test_rms_single_wave_grids_alternating_block_sizes(residual):
             assert np.array_equal(rout, ror)
 
 
+@pytest.mark.parametrize("H", [4096, 896])
+@pytest.mark.parametrize("ue8m0", [False, True], ids=["fp32", "ue8m0"])
+def test_rms_signed_zeros_and_underflowing_quotients(ue8m0, H):
+    """Signed zeros of x and of the weight give v = -0 or +0, whose codes are
+    0x80 and 0x00; negative subnormal inputs give quotients that underflow to
+    -0.  The quotient steps must keep those signs, per group and per token
+    (a CTA per row at H = 4096, a warp per row at H = 896)."""
+    import fp8_token_group_bf16_b300 as fq
+
+    T = 8
+    xb = inputs.bits(inputs.bf16(torch.randn(T, H, generator=torch.Generator().manual_seed(8800))))
+    xb[:, ::7] = 0x8000             # -0
+    xb[:, 3::7] = 0x0000            # +0
+    xb[1, 5::11] = 0x8001           # the smallest negative subnormal
+    xb[2, 6::13] = 0x0001
+    wb = inputs.bits(inputs.rms_weight(H))
+    wb[::13] |= 0x8000              # negative weights
+    wb[::17] = 0x8000               # -0 weights
+    q, s, _ = gpu_rms(xb, wb, None, ue8m0, False)
+    qr, sr, _, _, _ = oracle.rms_norm_per_block_quant(xb, wb, None, ue8m0=ue8m0)
+    assert_exact(q, s, qr, sr, f"signed zeros ue8m0={ue8m0}")
+    assert (qr == 0x80).any() and (qr == 0x00).any()
+    xd, wd = inputs.from_bits(xb).cuda(), inputs.from_bits(wb).cuda()
+    qt, st = fq.rms_norm_dynamic_per_token_quant(xd, wd, None, ue8m0=ue8m0)
+    torch.cuda.synchronize()
+    qtr, str_, _, _, _ = oracle.rms_norm_dynamic_per_token_quant(xb, wb, None, ue8m0=ue8m0)
+    assert np.array_equal(st.cpu().numpy().reshape(-1), str_)
+    assert np.array_equal(qt.view(torch.uint8).cpu().numpy(), qtr)
+
+
 @pytest.mark.parametrize("T,H", [(3, 24576), (512, 5120), (37, 1152), (2, 32768)])
 def test_rms_bit_exact_shapes(T, H):
     x = inputs.lognormal_channel_input(T, H, 6000 + T)
