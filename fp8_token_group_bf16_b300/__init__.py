@@ -56,6 +56,7 @@ EXPORTS = (
     "fp8q_f32_to_e4m3",
     "fp8q_silu_mul",
     "fp8q_group_scale",
+    "fp8q_quant_pairs",
     "fp8q_status_string",
     "fp8q_version",
 )
@@ -90,6 +91,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.fp8q_f32_to_e4m3.argtypes = [P, P, I64, P]
     L.fp8q_silu_mul.argtypes = [P, P, P, I64, P]
     L.fp8q_group_scale.argtypes = [P, P, I64, F, I32, P]
+    L.fp8q_quant_pairs.argtypes = [P, P, P, I64, P]
     for n in EXPORTS[:10]:
         getattr(L, n).restype = ctypes.c_int
     L.fp8q_status_string.argtypes = [ctypes.c_int]
@@ -149,6 +151,10 @@ def fp8q_silu_mul(a, b, out, n, stream):
 
 def fp8q_group_scale(amax, scales, n, eps, ue8m0, stream):
     return load().fp8q_group_scale(amax, scales, n, eps, ue8m0, stream)
+
+
+def fp8q_quant_pairs(v, s, out, n, stream):
+    return load().fp8q_quant_pairs(v, s, out, n, stream)
 
 
 def fp8q_status_string(status: int) -> str:
@@ -456,6 +462,25 @@ def group_scale(amax, eps: float = 1e-10, ue8m0: bool = False, out=None, stream=
         raise ValueError("out must be a contiguous fp32 tensor shaped like amax, on its device")
     _check(fp8q_group_scale(amax.data_ptr(), out.data_ptr(), amax.numel(), eps, int(ue8m0), _stream_ptr(amax, stream)),
            "group_scale")
+    return out
+
+
+def quant_pairs(v, s, out=None, stream=None):
+    """fp32 CUDA tensors of values and positive normal scales -> the
+    float8_e4m3fn codes e4m3(RN32(v / s)), by the kernels' quotient."""
+    torch = _torch()
+    for name, t in (("v", v), ("s", s)):
+        if t.device.type != "cuda" or t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous fp32 CUDA tensor")
+    _same_device("s", s, v)
+    if s.shape != v.shape:
+        raise ValueError("s must have v's shape")
+    if out is None:
+        out = torch.empty(v.shape, dtype=torch.uint8, device=v.device)
+    elif out.device != v.device or out.element_size() != 1 or out.numel() != v.numel() or not out.is_contiguous():
+        raise ValueError("out must be a contiguous 1-byte tensor with v's element count, on v's device")
+    _check(fp8q_quant_pairs(v.data_ptr(), s.data_ptr(), out.data_ptr(), v.numel(), _stream_ptr(v, stream)),
+           "quant_pairs")
     return out
 
 

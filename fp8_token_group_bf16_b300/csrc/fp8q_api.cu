@@ -657,6 +657,24 @@ int fp8q_group_scale(const float *amax, float *scales, int64_t n, float eps, int
     return launch_status(cudaSuccess);
 }
 
+int fp8q_quant_pairs(const float *v, const float *s, void *out, int64_t n, void *stream)
+{
+    if (n < 0)
+        return FP8Q_ERR_INVALID_ARG;
+    if (n == 0)
+        return FP8Q_OK;
+    if (!v || !s || !out)
+        return FP8Q_ERR_INVALID_ARG;
+    if (!aligned(v, 4) || !aligned(s, 4))
+        return FP8Q_ERR_MISALIGNED;
+    const int64_t blocks = (n + 255) / 256;
+    if (blocks > 0x7FFFFFFF)
+        return FP8Q_ERR_UNSUPPORTED;
+    quant_pairs_kernel<<<dim3{unsigned(blocks)}, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        v, s, static_cast<uint8_t *>(out), n);
+    return launch_status(cudaSuccess);
+}
+
 const char *fp8q_status_string(int status)
 {
     switch (status) {

@@ -294,15 +294,33 @@ __device__ __forceinline__ float group_scale(float amax, float eps)
     return div448_rn(a);
 }
 
-// 1/s: exact for a power of two (2^k has biased exponent k+127, 2^-k has
-// 127-k = 254 - that; s lies in [2^-108, 2^120] for finite inputs, so both
-// are normal), otherwise the correctly rounded reciprocal.
+// What quant8 needs of 1/s.  r: exact for a power of two (2^k has biased
+// exponent k+127, 2^-k has 127-k = 254 - that; s lies in [2^-108, 2^120] for
+// finite inputs, so both are normal), otherwise the correctly rounded
+// reciprocal.  For a non-power-of-two s also a split of 1/s into rd <= 1/s,
+// within one ulp, and rl = RN(1/s - rd) >= 0, so that rd + rl is 1/s to
+// within 2^-46 relative: with r = RN(1/s), the remainder 1 - s r is exact
+// (the residual of a faithful reciprocal is representable), so its sign says
+// whether r or its predecessor lies below 1/s; 1 - s rd >= 0 is exact for the
+// same reason, and rl = RN((1 - s rd) r).
+struct ScaleRecip {
+    float r, rd, rl;
+};
+
 template <bool UE8M0>
-__device__ __forceinline__ float scale_recip(float s)
+__device__ __forceinline__ ScaleRecip scale_recip(float s)
 {
-    if (UE8M0)
-        return __uint_as_float(0x7F000000u - (__float_as_uint(s) & 0x7F800000u));
-    return __frcp_rn(s);
+    ScaleRecip q;
+    if (UE8M0) {
+        q.r = __uint_as_float(0x7F000000u - (__float_as_uint(s) & 0x7F800000u));
+        q.rd = q.r;
+        q.rl = 0.0f;
+        return q;
+    }
+    q.r = __frcp_rn(s);
+    q.rd = __fmaf_rn(-s, q.r, 1.0f) < 0.0f ? __uint_as_float(__float_as_uint(q.r) - 1u) : q.r;
+    q.rl = __fmul_rn(__fmaf_rn(-s, q.rd, 1.0f), q.r);
+    return q;
 }
 
 // --------------------------------------------------------- packed fp32x2 ---
@@ -421,7 +439,7 @@ __device__ __forceinline__ uint32_t pack4_e4m3(float a0, float a1, float a2, flo
 }
 
 // Quantise 8 values (four packed pairs) with their group's scale s and
-// r = scale_recip(s) into 8 codes (c0: values 0-3, c1: values 4-7): each
+// rc = scale_recip(s) into 8 codes (c0: values 0-3, c1: values 4-7): each
 // code is e4m3(RN32(v / s)), the quotient correctly rounded.  The caller
 // passes w = v for a power-of-two scale (UE8M0) and w = -v otherwise (a sign
 // flip it gets for free or nearly: a negated factor, or bf16 inputs converted
@@ -429,36 +447,38 @@ __device__ __forceinline__ uint32_t pack4_e4m3(float a0, float a1, float a2, flo
 //
 // Power-of-two s: r is exactly 1/s, so one multiply is the exact quotient
 // rounded once (its sign, zero included, is the sign of v).
-// Otherwise: y0 = RN(v r) = RN(w (-r)) is within 1.5 ulp of v/s; one residual
-// step y1 = RN(y0 + RN(v - s y0) r) makes it faithful; a second step with the
-// exact residual v - s y1 (an FMA) then yields RN32(v/s) by Markstein's
+// Otherwise: y0 = RN(v rd + RN(v rl)) (two instructions, w (-rl) then
+// w (-rd) + that) is v/s (1 + d) rounded once with |d| < 2^-45, so it is
+// within 1/2 + 2^-21 ulp of v/s: faithful.  One step with the exact residual
+// v - s y0 (an FMA) and r = RN(1/s) then yields RN32(v/s) by Markstein's
 // theorem (P. Markstein, "Computation of elementary functions on the IBM
 // RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990: a faithful
 // quotient corrected with a correctly rounded reciprocal and an exact FMA
 // residual is the correctly rounded quotient, barring underflow).  Underflow
 // only happens for quotients far below 2^-10, whose e4m3 code is zero either
-// way.  Each step is taken as e = RN(s y + w) = -RN(v - s y) and
-// y' = RN(y + e (-r)), the same values (RN is symmetric), in an order that
-// keeps the sign of a zero quotient: for v = -0 (w = +0), y0 = -0,
-// e = RN(s (-0) + 0) = +0 and y' = RN(+0 (-r) + (-0)) = -0; for v = +0
-// every step gives +0; a quotient that underflows keeps the sign of v.
+// way.  The step is taken as e = RN(s y0 + w) = -RN(v - s y0) and
+// y1 = RN(y0 + e (-r)), the same values (RN is symmetric), in an order that
+// keeps the sign of a zero quotient: for v = -0 (w = +0), w (-rl) = -0
+// (rl >= 0), y0 = -0, e = RN(s (-0) + 0) = +0 and y1 = RN(+0 (-r) + (-0)) =
+// -0; for v = +0 every step gives +0; a quotient that underflows keeps the
+// sign of v.
 template <bool UE8M0>
-__device__ __forceinline__ void quant8(const uint64_t (&w)[4], float s, float r, uint32_t &c0, uint32_t &c1)
+__device__ __forceinline__ void quant8(const uint64_t (&w)[4], float s, const ScaleRecip &rc, uint32_t &c0,
+                                       uint32_t &c1)
 {
     float q[8];
     if (UE8M0) {
-        const uint64_t r2 = f2_pack(r, r);
+        const uint64_t r2 = f2_pack(rc.r, rc.r);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
             f2_unpack(f2_mul(w[k], r2), q[2 * k], q[2 * k + 1]);
     } else {
-        const uint64_t nr2 = f2_pack(-r, -r), s2 = f2_pack(s, s);
+        const uint64_t nr2 = f2_pack(-rc.r, -rc.r), nrd2 = f2_pack(-rc.rd, -rc.rd);
+        const uint64_t nrl2 = f2_pack(-rc.rl, -rc.rl), s2 = f2_pack(s, s);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            uint64_t y = f2_mul(w[k], nr2);
-            uint64_t e = f2_fma(s2, y, w[k]);
-            y = f2_fma(e, nr2, y);
-            e = f2_fma(s2, y, w[k]);
+            uint64_t y = f2_fma(w[k], nrd2, f2_mul(w[k], nrl2));
+            const uint64_t e = f2_fma(s2, y, w[k]);
             y = f2_fma(e, nr2, y);
             f2_unpack(y, q[2 * k], q[2 * k + 1]);
         }

@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(kGroupCtaThreads) group_quant_kernel(const uin
     }
     const float amax = quad_max(m);
     const float s = group_scale<UE8M0>(amax, eps);
-    const float r = scale_recip<UE8M0>(s);
+    const ScaleRecip r = scale_recip<UE8M0>(s);
     uint32_t codes[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kSiluCtaThreads, 16) silu_quant_kernel(const u
     }
     const float amax = quad_max(m);
     const float s = group_scale<UE8M0>(amax, eps);
-    const float r = scale_recip<UE8M0>(s);
+    const ScaleRecip r = scale_recip<UE8M0>(s);
     uint32_t codes[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -295,6 +295,25 @@ __global__ void __launch_bounds__(256) group_scale_kernel(const float *__restric
     const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i < n)
         out[i] = group_scale<UE8M0>(amax[i], eps);
+}
+
+// --------------------------------------------------------------------------
+// Elementwise e4m3(RN32(v / s)) for any positive normal fp32 scale s, by the
+// quotient every kernel takes for a non-power-of-two scale (for checking it
+// on its own over arbitrary fp32 values and scales).
+// --------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) quant_pairs_kernel(const float *__restrict__ v, const float *__restrict__ s,
+                                                          uint8_t *__restrict__ out, int64_t n)
+{
+    const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i < n) {
+        const float si = s[i], w = -v[i];   // quant8 takes -v
+        const uint64_t w2 = f2_pack(w, w);
+        const uint64_t w8[4] = {w2, w2, w2, w2};
+        uint32_t c0, c1;
+        quant8<false>(w8, si, scale_recip<false>(si), c0, c1);
+        out[i] = uint8_t(c0 & 0xFFu);
+    }
 }
 
 }  // namespace fp8q

@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(kRmsBlockMax<NG>, kRmsMinCtas<NG> * kRmsMaxThr
                 amax = fmaxf(amax, redm[i]);
         }
         const float sc = group_scale<UE8M0>(amax, kScaleFloor);
-        const float rc = scale_recip<UE8M0>(sc);
+        const ScaleRecip rc = scale_recip<UE8M0>(sc);
 
         // ---- pass 3: codes
 #pragma unroll
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(kRmsBlockMax<NG>, kRmsMinCtas<NG> * kRmsMaxThr
                 }
             const float amax = quad_max(fmaxf(mm[0], mm[1]));
             const float sc = group_scale<UE8M0>(amax, kScaleFloor);
-            const float rc = scale_recip<UE8M0>(sc);
+            const ScaleRecip rc = scale_recip<UE8M0>(sc);
             uint32_t codes[8];
 #pragma unroll
             for (int i = 0; i < 4; ++i)

@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(kRmsMaxThreads) rms_split_kernel(
         }
     const float amax = quad_max(fmaxf(mm[0], mm[1]));
     const float sc = group_scale<UE8M0>(amax, kScaleFloor);
-    const float rc = scale_recip<UE8M0>(sc);
+    const ScaleRecip rc = scale_recip<UE8M0>(sc);
     uint32_t codes[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i)

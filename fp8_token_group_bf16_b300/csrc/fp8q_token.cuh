@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(kCtaThreads, kTokenQuantMinCtas) token_quant_k
     const float amax = row_max_exchange(act ? m : 0.0f, part, rank, C);
 
     const float s = group_scale<UE8M0>(amax, eps);
-    const float rc = scale_recip<UE8M0>(s);
+    const ScaleRecip rc = scale_recip<UE8M0>(s);
     uint32_t codes[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(kCtaThreads, kTokenSiluMinCtas) token_silu_ker
     const float amax = row_max_exchange(act ? m : 0.0f, part, rank, C);
 
     const float s = group_scale<UE8M0>(amax, eps);
-    const float rc = scale_recip<UE8M0>(s);
+    const ScaleRecip rc = scale_recip<UE8M0>(s);
     uint32_t codes[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i)

@@ -258,6 +258,20 @@ FP8Q_API int fp8q_silu_mul(const float *a, const float *b, float *out, int64_t n
  */
 FP8Q_API int fp8q_group_scale(const float *amax, float *scales, int64_t n, float eps, int32_t ue8m0, void *stream);
 
+/*
+ * Elementwise quotient codes: out[i] = e4m3(RN32(v[i] / s[i])), the code of
+ * step A4 (quantise; "[RFC]: Using Helion for Selected vLLM CustomOps",
+ * Motivation, the Block_FP8 1x128 scheme) as every op above forms it for a
+ * scale that is not a power of two: the correctly rounded quotient from a
+ * faithful start and one exact-residual step, computed by the same device
+ * code.  Exposed so the quotient can be checked on its own over arbitrary
+ * fp32 values and scales.
+ *   v    fp32 [n], finite, read;  s  fp32 [n], positive and normal, with
+ *        |v[i] / s[i]| finite in fp32, read;  both 4-byte aligned.
+ *   out  float8_e4m3fn [n], written.
+ */
+FP8Q_API int fp8q_quant_pairs(const float *v, const float *s, void *out, int64_t n, void *stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 FP8Q_API const char *fp8q_status_string(int status);
 

@@ -182,6 +182,53 @@ def test_group_scale_every_fp32_significand():
             assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), (ue8m0, eps)
 
 
+def _quotient_pairs(rng, n_random=1 << 18, n_hard=20000):
+    """(v, s) pairs: scales RN32(amax / 448) over the binades with values up to
+    amax; pairs whose quotient lies within about 2^-47 (relative) of a
+    midpoint between two fp32 values (for an odd scale significand S and a
+    small odd t, N = 2^24 + (t S^-1 mod 2^24) makes S N = V 2^24 + t, so
+    v = V, s = S give v/s = N 2^-24 (1 - t / (S N)), scaled); signed zeros
+    and values whose quotient underflows."""
+    amax = (rng.uniform(1, 2, n_random) * 2.0 ** rng.integers(-60, 60, n_random)).astype(np.float32)
+    s = (amax.astype(np.float64) / 448).astype(np.float32)
+    v = (amax * rng.uniform(-1, 1, n_random)).astype(np.float32)
+    vs, ss = [v], [s]
+    hv, hs = [], []
+    mod = 1 << 24
+    while len(hv) < n_hard:
+        S = int(rng.integers(1 << 22, 1 << 23)) * 2 + 1
+        t = int(rng.choice([-3, -1, 1, 3]))
+        N = mod + (t * pow(S, -1, mod)) % mod
+        V = (S * N - t) // mod
+        if V >= mod:
+            continue
+        a = int(rng.integers(-40, 30))
+        shift = int(rng.choice([-9, -3, 0, 4, 7]))
+        sign = 1.0 if rng.random() < 0.5 else -1.0
+        hv.append(sign * float(V) * 2.0 ** (a - 23 + shift))
+        hs.append(float(S) * 2.0 ** (a - 23))
+    vs.append(np.array(hv, np.float32))
+    ss.append(np.array(hs, np.float32))
+    z = np.array([0.0, -0.0, 1e-45, -1e-45, 1e-40, -1e-40, 2.0 ** -126, -(2.0 ** -126)], np.float32)
+    vs.append(z)
+    ss.append(np.full(z.size, 3.0 / 448, np.float32))
+    return np.concatenate(vs), np.concatenate(ss)
+
+
+def test_quotient_of_arbitrary_fp32_values():
+    """The quotient every kernel takes for a non-power-of-two scale, on fp32
+    values (ops B and C quantise fp32 values, not bf16 ones), bit for bit
+    against the oracle's division, next to rounding midpoints included."""
+    import fp8_token_group_bf16_b300 as fq
+
+    v, s = _quotient_pairs(np.random.default_rng(15))
+    got = fq.quant_pairs(torch.from_numpy(v).cuda(), torch.from_numpy(s).cuda()).cpu().numpy()
+    want = oracle.quant_pairs(v, s)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, (bad.size, v[bad[:4]], s[bad[:4]], got[bad[:4]], want[bad[:4]])
+    assert (want == 0x80).any() and (want == 0x00).any()
+
+
 # ----------------------------------------------- op B (rms + quant) ----
 
 

@@ -199,6 +199,11 @@ def test_misaligned(lib):
     assert fq.fp8q_group_scale(A, A, 16, 0.0, 0, None) == fq.FP8Q_ERR_INVALID_ARG
     assert fq.fp8q_group_scale(None, A, 16, 1e-10, 1, None) == fq.FP8Q_ERR_INVALID_ARG
     assert fq.fp8q_group_scale(None, None, 0, 1e-10, 0, None) == 0
+    assert fq.fp8q_quant_pairs(A + 2, A, Q, 16, None) == M
+    assert fq.fp8q_quant_pairs(A, A + 2, Q, 16, None) == M
+    assert fq.fp8q_quant_pairs(A, A, Q, -1, None) == fq.FP8Q_ERR_INVALID_ARG
+    assert fq.fp8q_quant_pairs(A, None, Q, 16, None) == fq.FP8Q_ERR_INVALID_ARG
+    assert fq.fp8q_quant_pairs(None, None, None, 0, None) == 0
 
 
 def test_empty_input_is_a_no_op(lib):
