@@ -168,6 +168,10 @@ __global__ void __launch_bounds__(kRopeCtaThreads, kRopeMinCtas) qk_norm_rope_ke
         pair_add(hi, lo, __shfl_xor_sync(0xFFFFFFFFu, hi, o), __shfl_xor_sync(0xFFFFFFFFu, lo, o));
     const float inv = rms_inv(hi, lo, kHeadDim, eps);
     const uint64_t inv2 = f2_pack(inv, inv);
+    // -0, formed at run time (eps is finite, so eps * 0 is +0): the addend of
+    // the rotation's products below
+    const float nzf = -__fmul_rn(eps, 0.0f);
+    const uint64_t nz2 = f2_pack(nzf, nzf);
 
     // ---- y = (z * inv) * w, then the rotation of each (a, b) pair
     uint32_t out[NW];
@@ -192,19 +196,30 @@ __global__ void __launch_bounds__(kRopeCtaThreads, kRopeMinCtas) qk_norm_rope_ke
             a = f2_pack(a0, a1);
             b = f2_pack(b0, b1);
         }
-        // The rotation in scalar IEEE intrinsics: the code generator may fuse a
-        // packed multiply into a following packed add or subtract (one
-        // rounding instead of two), which __fmul_rn / __fadd_rn / __fsub_rn
-        // are guaranteed never to be.
-        float ya0, ya1, yb0, yb1, c0, c1, s0, s1;
-        f2_unpack(a, ya0, ya1);
-        f2_unpack(b, yb0, yb1);
-        f2_unpack(c, c0, c1);
-        f2_unpack(s, s0, s1);
-        const float a0 = __fsub_rn(__fmul_rn(ya0, c0), __fmul_rn(yb0, s0));
-        const float a1 = __fsub_rn(__fmul_rn(ya1, c1), __fmul_rn(yb1, s1));
-        const float b0 = __fadd_rn(__fmul_rn(yb0, c0), __fmul_rn(ya0, s0));
-        const float b1 = __fadd_rn(__fmul_rn(yb1, c1), __fmul_rn(ya1, s1));
+        float a0, a1, b0, b1;
+        if (NEOX) {
+            // The rotation in packed instructions, each product an FMA with a
+            // -0 addend that the code generator cannot see: RN(x y + (-0)) =
+            // RN(x y), signed zeros included, and an FMA's result is never
+            // fused into the add or subtract that follows.  (A packed multiply
+            // was: one rounding instead of two.)
+            const uint64_t ac = f2_fma(a, c, nz2), bs = f2_fma(b, s, nz2);
+            const uint64_t bc = f2_fma(b, c, nz2), as = f2_fma(a, s, nz2);
+            f2_unpack(f2_sub(ac, bs), a0, a1);
+            f2_unpack(f2_add(bc, as), b0, b1);
+        } else {
+            // Interleaved pairs (repacked above; the packed form spills
+            // here): scalar IEEE intrinsics, which are never fused.
+            float ya0, ya1, yb0, yb1, c0, c1, s0, s1;
+            f2_unpack(a, ya0, ya1);
+            f2_unpack(b, yb0, yb1);
+            f2_unpack(c, c0, c1);
+            f2_unpack(s, s0, s1);
+            a0 = __fsub_rn(__fmul_rn(ya0, c0), __fmul_rn(yb0, s0));
+            a1 = __fsub_rn(__fmul_rn(ya1, c1), __fmul_rn(yb1, s1));
+            b0 = __fadd_rn(__fmul_rn(yb0, c0), __fmul_rn(ya0, s0));
+            b1 = __fadd_rn(__fmul_rn(yb1, c1), __fmul_rn(ya1, s1));
+        }
         if (NEOX) {
             out[k] = bf16x2_rn(a0, a1);
             out[NWP + k] = bf16x2_rn(b0, b1);
