@@ -151,8 +151,12 @@ __global__ void __launch_bounds__(kRmsBlockMax<NG>, kRmsMinCtas<NG> * kRmsMaxThr
             uint32_t r[16];
             ld64_rw<V8>(residual + rbase + off, r);
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-                z[j][e] = pack_bf16x2(__fadd_rn(bf_lo(z[j][e]), bf_lo(r[e])), __fadd_rn(bf_hi(z[j][e]), bf_hi(r[e])));
+            for (int e = 0; e < 16; ++e) {
+                // x + r for both halves in one packed add (no product near it to fuse)
+                float lo, hi;
+                f2_unpack(f2_add(f2_from_bf16x2(z[j][e]), f2_from_bf16x2(r[e])), lo, hi);
+                z[j][e] = pack_bf16x2(lo, hi);
+            }
         }
         ld64_keep_l1<V8>(w + off, wr[j]);
     }
