@@ -182,9 +182,13 @@ template <int NG, bool U, int C, bool R, bool V>
 cudaError_t launch_rms_row(const uint16_t *x, uint16_t *res, const uint16_t *w, uint8_t *q, float *s, int T,
                            int H, int G, float eps, cudaStream_t st)
 {
-    // rows of at most kRmsWarpRowGroups groups: a warp each, kRmsWarpRowsPerCta
-    // rows per CTA; longer rows: a CTA each
+    // Rows of at most kRmsWarpRowGroups groups: a warp each, kRmsWarpRowsPerCta
+    // rows per CTA; rows of more than 64 groups, one group per quad: a wide
+    // CTA each (up to 1024 threads); the rest: a CTA each.
+    constexpr int kWarp = NG == 1 ? kRmsWarpRow : kRmsCtaRow;
+    constexpr int kWide = NG == 1 ? kRmsWideRow : kRmsCtaRow;
     const bool wpr = NG == 1 && G <= kRmsWarpRowGroups;
+    const bool wide = NG == 1 && G > 64;
     const int rpc = wpr ? kRmsWarpRowsPerCta : 1;
     const int quads = (G + NG - 1) / NG;
     const int threads = wpr ? 32 * rpc : ((quads * 4 + 31) / 32) * 32;
@@ -197,14 +201,20 @@ cudaError_t launch_rms_row(const uint16_t *x, uint16_t *res, const uint16_t *w, 
         if (int64_t(T) >
             int64_t(sms) * rpc * resident_per_sm(threads, 65536 / (kRmsMaxThreads * kRmsMinCtas<NG>))) {
             if (wpr)
-                return launch(rms_row_kernel<NG, U, C, R, V, true, NG == 1>, grid, block, st, x, res, w, q, s, T, H,
+                return launch(rms_row_kernel<NG, U, C, R, V, true, kWarp>, grid, block, st, x, res, w, q, s, T, H,
                               G, eps, sms * 3 / 2 * rpc);
+            if (wide)
+                return launch(rms_row_kernel<NG, U, C, R, V, true, kWide>, grid, block, st, x, res, w, q, s, T, H,
+                              G, eps, sms * 3 / 2);
             return launch(rms_row_kernel<NG, U, C, R, V, true>, grid, block, st, x, res, w, q, s, T, H, G, eps,
                           sms * 3 / 2);
         }
     }
     if (wpr)
-        return launch(rms_row_kernel<NG, U, C, R, V, false, NG == 1>, grid, block, st, x, res, w, q, s, T, H, G,
+        return launch(rms_row_kernel<NG, U, C, R, V, false, kWarp>, grid, block, st, x, res, w, q, s, T, H, G,
+                      eps, 0);
+    if (wide)
+        return launch(rms_row_kernel<NG, U, C, R, V, false, kWide>, grid, block, st, x, res, w, q, s, T, H, G,
                       eps, 0);
     // A single wave: spread evenly over the SMs.  The CTA scheduler does not
     // deal a one-wave grid out evenly: some SMs take as many CTAs as fit while
@@ -279,11 +289,22 @@ cudaError_t launch_rms(const uint16_t *x, uint16_t *res, const uint16_t *w, uint
 #define FP8Q_ROW(NG)                                                                             \
     (v8 ? launch_rms_row<NG, U, C, R, true>(x, res, w, q, s, T, H, G, eps, st)                  \
         : launch_rms_row<NG, U, C, R, false>(x, res, w, q, s, T, H, G, eps, st))
+    // One group per quad (a wide CTA of up to 1024 threads above 64 groups)
+    // for every row with per-group scales; measured against 2 and 4 groups per quad (256-thread
+    // CTAs holding 64 and 128 values a thread), UE8M0 row-major, us: H = 24576,
+    // T = 8192 169.0 / 196.7; H = 8320, T = 8192 49.7 / 51.9; H = 32768,
+    // T = 8192 215.1 / 226.0; H = 16384, T = 8192 91.6 / 90.0.  The
+    // per-token scale keeps 2 and 4 groups per quad (31.2 / 30.3 us at
+    // H = 16384, T = 2048 with one).
     if (G <= 64)
         return FP8Q_ROW(1);
-    if (G <= 128)
-        return FP8Q_ROW(2);
-    return FP8Q_ROW(4);
+    if constexpr (C != kPerToken) {
+        return FP8Q_ROW(1);
+    } else {
+        if (G <= 128)
+            return FP8Q_ROW(2);
+        return FP8Q_ROW(4);
+    }
 #undef FP8Q_ROW
 }
 

@@ -21,18 +21,25 @@
 
 namespace fp8q {
 
-// Threads that own groups: at most 64 quads.
+// Threads that own groups with 2 or 4 groups per quad (the per-token
+// scale's rows of more than 64 groups): at most 64 quads.
 constexpr int kRmsMaxThreads = 256;
 // CTAs of kRmsMaxThreads per SM that the register cap allows: NG groups per
 // quad hold 32 NG values and as many weights in registers (64, 128 and 255
 // registers a thread).
 template <int NG>
 constexpr int kRmsMinCtas = NG == 1 ? 4 : (NG == 2 ? 2 : 1);
-// The largest block the host may launch: with one group per quad it may pad
-// a CTA with warps that own no group, so that fewer CTAs fit a SM (the
-// launch bounds keep the same register cap).
+// The largest block the host may launch: with one group per quad, a row of
+// up to 256 groups, or a CTA padded with warps that own no group so that
+// fewer CTAs fit a SM (the launch bounds keep the same register cap).
 template <int NG>
 constexpr int kRmsBlockMax = NG == 1 ? 2 * kRmsMaxThreads : kRmsMaxThreads;
+// The shapes of a row's work: a CTA per row (up to 64 groups, or 2 or 4
+// groups per quad); a warp per row, several rows per CTA (up to 8 groups);
+// a wide CTA per row, one group per quad (65 to 256 groups: up to 1024
+// threads, 32 warps, whose partial sums meet in a butterfly).
+constexpr int kRmsCtaRow = 0, kRmsWarpRow = 1, kRmsWideRow = 2;
+constexpr int kRmsWideBlockMax = 1024;
 // Rows of at most this many groups take a warp each, this many rows per CTA.
 constexpr int kRmsWarpRowGroups = 8;
 constexpr int kRmsWarpRowsPerCta = 4;
@@ -86,8 +93,10 @@ __device__ __forceinline__ float rms_inv(float hi, float lo, int H, float eps)
 
 // ------------------------------------------------------------- kernel ---
 //
-// One CTA per row (grid = T), one quad per group (NG groups per quad for
-// rows of more than 64 groups): every lane loads its 32 * NG values and its
+// One CTA per row (grid = T), one quad per group (NG = 2 or 4 groups per
+// quad for the per-token scale's rows of more than 64 groups; with per-group
+// scales a row of up to 256 groups takes a CTA of up to 1024 threads, whose
+// warps' partial sums meet in a butterfly above 8 warps): every lane loads its 32 * NG values and its
 // 32 * NG weights straight into registers with 256-bit loads (128-bit when
 // the buffers are only 16-byte aligned), so the row is read from HBM once and
 // stays in registers between the sum of squares and the quantisation.  Each
@@ -116,20 +125,22 @@ __device__ __forceinline__ float rms_inv(float hi, float lo, int H, float eps)
 // against 20.0 us at T = 4096, H = 5120 for forming v a second time from z
 // and w after the barrier.
 
-template <int NG, bool UE8M0, int LAYOUT, bool RES, bool V8, bool PF, bool WPR = false>
-__global__ void __launch_bounds__(kRmsBlockMax<NG>, kRmsMinCtas<NG> * kRmsMaxThreads / kRmsBlockMax<NG>)
+template <int NG, bool UE8M0, int LAYOUT, bool RES, bool V8, bool PF, int ROWS = kRmsCtaRow>
+__global__ void __launch_bounds__(ROWS == kRmsWideRow ? kRmsWideBlockMax : kRmsBlockMax<NG>,
+                                  ROWS == kRmsWideRow ? 1 : kRmsMinCtas<NG> * kRmsMaxThreads / kRmsBlockMax<NG>)
     rms_row_kernel(const uint16_t *__restrict__ x, uint16_t *__restrict__ residual, const uint16_t *__restrict__ w,
                    uint8_t *__restrict__ q, float *__restrict__ scales, int T, int H, int G, float eps, int pf)
 {
-    __shared__ float2 red[kRmsMaxThreads / 32];
-    __shared__ float redm[kRmsMaxThreads / 32];
+    constexpr int kWarps = ROWS == kRmsWideRow ? kRmsWideBlockMax / 32 : kRmsMaxThreads / 32;
+    __shared__ float2 red[kWarps];
+    __shared__ float redm[kWarps];
     const int tid = threadIdx.x, lane = tid & 31, sub = tid & 3, warp = tid >> 5;
-    // WPR (rows of at most kRmsWarpRowGroups groups): a warp per row,
-    // blockDim.x / 32 rows per CTA.  Otherwise a CTA per row, whose threads
-    // that own groups are ceil(G / NG) quads in whole warps; warps beyond
-    // them only pad the CTA and leave at once.
-    static_assert(!WPR || NG == 1, "a warp holds one group per quad");
-    constexpr bool wpr = WPR;
+    // kRmsWarpRow (rows of at most kRmsWarpRowGroups groups): a warp per
+    // row, blockDim.x / 32 rows per CTA.  Otherwise a CTA per row, whose
+    // threads that own groups are ceil(G / NG) quads in whole warps; warps
+    // beyond them only pad the CTA and leave at once.
+    static_assert(ROWS == kRmsCtaRow || NG == 1, "warp and wide rows hold one group per quad");
+    constexpr bool wpr = ROWS == kRmsWarpRow;
     const int nthr = wpr ? 32 : (((G + NG - 1) / NG * 4 + 31) >> 5) << 5;
     const int row = wpr ? int(blockIdx.x) * int(blockDim.x >> 5) + warp : int(blockIdx.x);
     if ((!wpr && tid >= nthr) || row >= T)
@@ -196,9 +207,19 @@ __global__ void __launch_bounds__(kRmsBlockMax<NG>, kRmsMinCtas<NG> * kRmsMaxThr
         if (lane == 0)
             red[warp] = a;
         bar_sync_first(nthr);
-        a = red[0];
-        for (int i = 1; i < nwarps; ++i)
-            pair_add(a.x, a.y, red[i].x, red[i].y);
+        if constexpr (ROWS == kRmsWideRow) {
+            // up to 32 warps: each warp reads the pairs one a lane and forms
+            // the same total with a butterfly (every lane of every warp ends
+            // with the same pair, as above)
+            a = lane < nwarps ? red[lane] : make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int o = 1; o <= 16; o <<= 1)
+                pair_add(a.x, a.y, __shfl_xor_sync(0xFFFFFFFFu, a.x, o), __shfl_xor_sync(0xFFFFFFFFu, a.y, o));
+        } else {
+            a = red[0];
+            for (int i = 1; i < nwarps; ++i)
+                pair_add(a.x, a.y, red[i].x, red[i].y);
+        }
     }
     const float inv = rms_inv(a.x, a.y, H, eps);
     // With an fp32 scale the normalised values are formed negated (exactly:
