@@ -417,7 +417,9 @@ def test_rms_signed_zeros_and_underflowing_quotients(ue8m0, H):
     assert np.array_equal(qt.view(torch.uint8).cpu().numpy(), qtr)
 
 
-@pytest.mark.parametrize("T,H", [(3, 24576), (512, 5120), (37, 1152), (2, 32768)])
+@pytest.mark.parametrize("T,H", [(3, 24576), (512, 5120), (37, 1152), (2, 32768),
+                                 # wide CTAs (65 to 256 groups), one wave and the prefetching build
+                                 (100, 8320), (300, 24576), (150, 32768)])
 def test_rms_bit_exact_shapes(T, H):
     x = inputs.lognormal_channel_input(T, H, 6000 + T)
     w = inputs.rms_weight(H)
