@@ -182,11 +182,20 @@ template <int NG, bool U, int C, bool R, bool V>
 cudaError_t launch_rms_row(const uint16_t *x, uint16_t *res, const uint16_t *w, uint8_t *q, float *s, int T,
                            int H, int G, float eps, cudaStream_t st)
 {
-    // Rows of at most kRmsWarpRowGroups groups: a warp each, kRmsWarpRowsPerCta
-    // rows per CTA; rows of more than 64 groups, one group per quad: a wide
-    // CTA each (up to 1024 threads); the rest: a CTA each.
+    // Rows of 1, 2 or 4 groups: 8, 4 or 2 to a warp, kRmsWarpRowsPerCta warps
+    // per CTA (at T = 65536, against a warp per row: H = 128 6.97 / 34.4 us,
+    // H = 256 11.8 / 34.5, H = 512 20.9 / 34.6); rows of at most kRmsWarpRowGroups
+    // groups: a warp each, kRmsWarpRowsPerCta rows per CTA; rows of more
+    // than 64 groups, one group per quad: a wide CTA each (up to 1024
+    // threads); the rest: a CTA each.
     constexpr int kWarp = NG == 1 ? kRmsWarpRow : kRmsCtaRow;
     constexpr int kWide = NG == 1 ? kRmsWideRow : kRmsCtaRow;
+    constexpr int kSub = NG == 1 ? kRmsSubWarpRow : kRmsCtaRow;
+    if (NG == 1 && (G == 1 || G == 2 || G == 4)) {
+        const int rows_per_cta = kRmsWarpRowsPerCta * (8 / G);
+        return launch(rms_row_kernel<NG, U, C, R, V, false, kSub>, dim3{unsigned((T + rows_per_cta - 1) / rows_per_cta)},
+                      dim3{unsigned(32 * kRmsWarpRowsPerCta)}, st, x, res, w, q, s, T, H, G, eps, 0);
+    }
     const bool wpr = NG == 1 && G <= kRmsWarpRowGroups;
     const bool wide = NG == 1 && G > 64;
     const int rpc = wpr ? kRmsWarpRowsPerCta : 1;

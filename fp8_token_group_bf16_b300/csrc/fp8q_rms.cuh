@@ -38,7 +38,8 @@ constexpr int kRmsBlockMax = NG == 1 ? 2 * kRmsMaxThreads : kRmsMaxThreads;
 // groups per quad); a warp per row, several rows per CTA (up to 8 groups);
 // a wide CTA per row, one group per quad (65 to 256 groups: up to 1024
 // threads, 32 warps, whose partial sums meet in a butterfly).
-constexpr int kRmsCtaRow = 0, kRmsWarpRow = 1, kRmsWideRow = 2;
+// Rows of 1, 2 or 4 groups: several to a warp (kRmsSubWarpRow), 4 G lanes each.
+constexpr int kRmsCtaRow = 0, kRmsWarpRow = 1, kRmsWideRow = 2, kRmsSubWarpRow = 3;
 constexpr int kRmsWideBlockMax = 1024;
 // Rows of at most this many groups take a warp each, this many rows per CTA.
 constexpr int kRmsWarpRowGroups = 8;
@@ -136,18 +137,27 @@ __global__ void __launch_bounds__(ROWS == kRmsWideRow ? kRmsWideBlockMax : kRmsB
     __shared__ float redm[kWarps];
     const int tid = threadIdx.x, lane = tid & 31, sub = tid & 3, warp = tid >> 5;
     // kRmsWarpRow (rows of at most kRmsWarpRowGroups groups): a warp per
-    // row, blockDim.x / 32 rows per CTA.  Otherwise a CTA per row, whose
-    // threads that own groups are ceil(G / NG) quads in whole warps; warps
-    // beyond them only pad the CTA and leave at once.
+    // row, blockDim.x / 32 rows per CTA.  kRmsSubWarpRow (rows of 1, 2 or 4
+    // groups): 32 / (4 G) rows per warp, each on a segment of 4 G lanes whose
+    // reductions stay inside it; a lane whose row lies past T works on a copy
+    // of row T - 1 (its segment still takes part in the shuffles) and stores
+    // nothing.  Otherwise a CTA per row, whose threads that own groups are
+    // ceil(G / NG) quads in whole warps; warps beyond them only pad the CTA
+    // and leave at once.
     static_assert(ROWS == kRmsCtaRow || NG == 1, "warp and wide rows hold one group per quad");
-    constexpr bool wpr = ROWS == kRmsWarpRow;
+    static_assert(!(PF && ROWS == kRmsSubWarpRow), "no prefetching build for rows several to a warp");
+    constexpr bool subw = ROWS == kRmsSubWarpRow;
+    constexpr bool wpr = ROWS == kRmsWarpRow || subw;
+    const int lpr = subw ? 4 * G : 32;   // lanes of a row's reductions (a power of two)
     const int nthr = wpr ? 32 : (((G + NG - 1) / NG * 4 + 31) >> 5) << 5;
-    const int row = wpr ? int(blockIdx.x) * int(blockDim.x >> 5) + warp : int(blockIdx.x);
-    if ((!wpr && tid >= nthr) || row >= T)
+    const int wrow = int(blockIdx.x) * int(blockDim.x >> 5) + warp;   // the CTA-wide warp index
+    const int row = subw ? wrow * (32 / lpr) + lane / lpr : (wpr ? wrow : int(blockIdx.x));
+    if (subw ? wrow * (32 / lpr) >= T : ((!wpr && tid >= nthr) || row >= T))
         return;
-    const int quad = (wpr ? lane : tid) >> 2;
-    const int nq = nthr >> 2, nwarps = nthr >> 5;
-    const int64_t rbase = int64_t(row) * H;
+    const bool live = row < T;
+    const int quad = (wpr ? (subw ? lane & (lpr - 1) : lane) : tid) >> 2;
+    const int nq = subw ? G : nthr >> 2, nwarps = nthr >> 5;
+    const int64_t rbase = int64_t(live ? row : T - 1) * H;
 
     wait_for_producer();
     allow_consumer_launch();
@@ -182,7 +192,7 @@ __global__ void __launch_bounds__(ROWS == kRmsWideRow ? kRmsWideBlockMax : kRmsB
 #pragma unroll
         for (int j = 0; j < NG; ++j) {
             const int g = quad + nq * j;
-            if (g < G)
+            if (g < G && live)
                 st64<V8>(residual + rbase + g * kGroup + sub * kValsPerLane, z[j]);
         }
     }
@@ -198,7 +208,8 @@ __global__ void __launch_bounds__(ROWS == kRmsWideRow ? kRmsWideBlockMax : kRmsB
     }
 #pragma unroll
     for (int o = 1; o <= 16; o <<= 1)
-        pair_add(hi, lo, __shfl_xor_sync(0xFFFFFFFFu, hi, o), __shfl_xor_sync(0xFFFFFFFFu, lo, o));
+        if (o < lpr)
+            pair_add(hi, lo, __shfl_xor_sync(0xFFFFFFFFu, hi, o), __shfl_xor_sync(0xFFFFFFFFu, lo, o));
     // One warp: every lane holds the same pair (pair_add is symmetric, so both
     // partners of each butterfly step form the same sum).  Several: one
     // barrier, then every thread adds the warps' pairs in the same order.
@@ -245,7 +256,8 @@ __global__ void __launch_bounds__(ROWS == kRmsWideRow ? kRmsWideBlockMax : kRmsB
         float m = fmaxf(mm[0], mm[1]);
 #pragma unroll
         for (int o = 1; o <= 16; o <<= 1)
-            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+            if (o < lpr)
+                m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
         float amax = m;
         if (nwarps > 1) {
             if (lane == 0)
@@ -267,10 +279,10 @@ __global__ void __launch_bounds__(ROWS == kRmsWideRow ? kRmsWideBlockMax : kRmsB
             for (int i = 0; i < 4; ++i)
                 quant8<UE8M0>(*reinterpret_cast<const uint64_t(*)[4]>(&v[j][4 * i]), sc, rc, codes[2 * i],
                               codes[2 * i + 1]);
-            if (g < G)
+            if (g < G && live)
                 st32<V8>(q + rbase + g * kGroup + sub * kValsPerLane, codes);
         }
-        if ((wpr ? lane : tid) == 0)
+        if ((wpr ? lane & (lpr - 1) : tid) == 0 && live)
             scales[row] = sc;
     } else {
         // ---- pass 2: v = (z * inv) * w, group scale, codes
@@ -296,7 +308,7 @@ __global__ void __launch_bounds__(ROWS == kRmsWideRow ? kRmsWideBlockMax : kRmsB
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 quant8<UE8M0>(v[i], sc, rc, codes[2 * i], codes[2 * i + 1]);
-            if (g < G) {
+            if (g < G && live) {
                 st32<V8>(q + rbase + g * kGroup + sub * kValsPerLane, codes);
                 if (sub == 0)
                     store_scale<LAYOUT>(scales, sc, row, g, T, G);

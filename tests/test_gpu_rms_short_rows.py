@@ -2,12 +2,13 @@
 groups, through the C ABI, bit for bit against the oracle.
 
 Such a row fits one warp (one quad per group), so the kernel gives each row
-a warp of a CTA of several rows and forms the row's sum from the warp's
+a warp of a CTA of several rows (rows of 1, 2 or 4 groups: 8, 4 or 2 rows
+to a warp, each on its own segment of lanes) and forms the row's sum from a
 butterfly alone, with no shared memory and no barrier.  Covered: T that
-leave the last CTA partly without rows (1, 3, 5, 127, 1001), a grid long
-enough for the build that hands later rows to the L2 (6000 rows at
-H = 1024), rows of 1, 3, 7 and 8 groups (a warp partly idle for the
-shorter ones), with and without the residual, in every scale layout.
+leave the last CTA or the last warp partly without rows (1, 3, 5, 127,
+1001), a grid long enough for the build that hands later rows to the L2
+(6000 rows at H = 1024), rows of 1 to 8 groups, with and without the
+residual, in every scale layout.
 """
 
 import numpy as np
@@ -23,7 +24,7 @@ from tolerance import assert_exact, to_tg
 pytestmark = pytest.mark.gpu
 
 T_VALUES = [1, 3, 5, 127, 1001, 6000]
-H_VALUES = [128, 384, 896, 1024]
+H_VALUES = [128, 256, 384, 512, 896, 1024]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -77,7 +78,7 @@ def test_rms_short_rows_bit_exact(T, H, residual):
 
 
 @pytest.mark.parametrize("T,H,residual", [(1, 128, True), (5, 896, False), (127, 1024, True), (6000, 1024, False),
-                                          (1001, 384, False)])
+                                          (1001, 384, False), (77, 256, True), (1001, 512, False), (33, 128, False)])
 @pytest.mark.parametrize("ue8m0", [False, True], ids=["fp32", "ue8m0"])
 def test_rms_per_token_short_rows_bit_exact(T, H, residual, ue8m0):
     x, w, r = inputs.rms_input(T, H, seeds=(9200 + T, 9201 + H, 9202))
@@ -97,7 +98,8 @@ def test_rms_per_token_short_rows_bit_exact(T, H, residual, ue8m0):
 
 
 def test_rms_short_rows_degenerate():
-    """All-zero, constant and tiny rows of one group, a warp each."""
+    """All-zero, constant and tiny rows of one group, eight to a warp (six
+    rows: the warp's last two segments lie past T)."""
     H = 128
     x = torch.zeros(6, H)
     x[1] = 0.75
