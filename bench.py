@@ -850,6 +850,7 @@ def _sweep_points(fq, dev, peak, peak_kind):
     points.append(("silu_and_mul_per_block_quant", 1024, 12288, True, "col", False))
     for T in (4096, 16384):   # short rows: a warp per row
         points.append(("rms_norm_per_block_quant", T, 1024, True, "row", False))
+    points.append(("rms_norm_per_block_quant", 65536, 128, True, "row", False))   # eight rows to a warp
     for H in (16384, 32768):   # long rows: a wide CTA per row
         points.append(("rms_norm_per_block_quant", 4096, H, True, "row", False))
     for T in (512, 4096):   # packed UE8M0 exponent bytes, and the same bytes in MXFP8 GEMM tiles
