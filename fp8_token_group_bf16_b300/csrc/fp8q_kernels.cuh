@@ -238,7 +238,14 @@ __global__ void __launch_bounds__(kSiluCtaThreads, 16) silu_quant_kernel(const u
 #pragma unroll
     for (int i = 0; i < 4; ++i)
         quant8<UE8M0>(*reinterpret_cast<const uint64_t(*)[4]>(&v[4 * i]), s, r, codes[2 * i], codes[2 * i + 1]);
-    if (ok) {
+    if constexpr (LAYOUT == kPackedUe8m0) {
+        // a CTA starts at a multiple of 16 groups, so each half warp's four
+        // quads own four 4-aligned consecutive groups
+        const PackedQuads pw = packed_quads_gather(s, ok, t, g, T, G);
+        if (ok)
+            st32<V8>(q + gi * kGroup + sub * kValsPerLane, codes);
+        packed_quads_store(scales, pw, s, ok, sub, t, g, T, G);
+    } else if (ok) {
         st32<V8>(q + gi * kGroup + sub * kValsPerLane, codes);
         if (sub == 0)
             store_scale<LAYOUT>(scales, s, t, g, T, G);

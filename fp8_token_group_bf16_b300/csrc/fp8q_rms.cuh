@@ -308,6 +308,9 @@ __global__ void __launch_bounds__(ROWS == kRmsWideRow ? kRmsWideBlockMax : kRmsB
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 quant8<UE8M0>(v[i], sc, rc, codes[2 * i], codes[2 * i + 1]);
+            // (packed exponent bytes a byte per group: gathering each word of
+            // four from the quads, as op C does, measured slower here, 14.93
+            // against 14.44 us at T = 4096, H = 5120)
             if (g < G && live) {
                 st32<V8>(q + rbase + g * kGroup + sub * kValsPerLane, codes);
                 if (sub == 0)
